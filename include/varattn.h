@@ -1,0 +1,202 @@
+/*
+ * varattn -- the attention hot path of next-scale visual autoregressive (VAR)
+ * generation on NVIDIA B300 (sm_103a), as a C ABI.
+ *
+ * At scale step k the queries of the current s_k x s_k token grid attend over
+ * a KV cache that holds every token of scales 1..k ("SparVAR: Exploring
+ * Sparsity in Visual AutoRegressive Modeling", abstract: each step attends to
+ * all tokens across historical scales; "ARVAR", Background & Motivation: KV
+ * caching).  Tokens of one scale are stored row-major (flat index r*s + c) and
+ * the scales are concatenated in schedule order.
+ *
+ * Conventions shared by every entry point:
+ *  - Tensors are bf16, dense row-major, no padding unless a field says so:
+ *      Q, O            [B][H][N][D]             N = side[step]^2
+ *      K, V            [B][H][kv_capacity][D]   first L rows used,
+ *                                               L = sum_{i<=step} side[i]^2
+ *  - Pointers to tensors are DEVICE pointers owned by the caller; the library
+ *    never allocates, frees or retains them.  Pointers must be 16-byte aligned.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  No call synchronises the device except
+ *    var_device_status().
+ *  - Return value: a var_status code.  Arguments are checked on the host before
+ *    any launch; a failing check launches nothing.  Faults detected on the
+ *    device (a pipeline wait that timed out) are recorded in a device status
+ *    word read by var_device_status().
+ *  - No C++ exception crosses this interface.
+ */
+#ifndef VARATTN_H
+#define VARATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define VAR_API __attribute__((visibility("default")))
+#else
+#define VAR_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    VAR_OK = 0,
+    VAR_ERR_INVALID_ARG = 1,  /* a null pointer, a size out of range, bad indices */
+    VAR_ERR_UNSUPPORTED = 2,  /* head_dim not 64/128, misaligned pointer, shape limit */
+    VAR_ERR_CUDA = 3,         /* a CUDA runtime call failed (launch, attribute, ...) */
+    VAR_ERR_TIMEOUT = 4,      /* a device pipeline wait gave up (device status word) */
+    VAR_ERR_NUMERIC = 5,      /* input outside the exactly-handled range (pivot select) */
+    VAR_ERR_WORKSPACE = 6     /* workspace missing or smaller than required */
+} var_status;
+
+#define VAR_MAX_SCALES 32
+
+/* The problem statement: the scale schedule, heads, head_dim, CFG batch. */
+typedef struct {
+    int32_t batch;        /* B: 2 for a classifier-free-guidance (cond, uncond) pair */
+    int32_t heads;        /* H */
+    int32_t head_dim;     /* D: 64 or 128 */
+    int32_t n_scales;     /* number of entries of side[] in use, 1..VAR_MAX_SCALES */
+    int32_t side[VAR_MAX_SCALES]; /* s_1..s_n: side lengths of the token grids */
+    int32_t kv_capacity;  /* rows per (b,h) in the K/V buffers; 0 = exactly L(step) */
+    float softmax_scale;  /* 0 = 1/sqrt(head_dim) */
+} var_problem;
+
+/*
+ * Dense cross-scale attention at scale index `step` (0-based):
+ *   O[b,h,i,:] = sum_{j<L} softmax_j(Q[b,h,i,:] . K[b,h,j,:] * scale) V[b,h,j,:]
+ * for every query i < N of the current grid, over all L cached tokens of scales
+ * 0..step with no mask inside the step (SparVAR abstract).  fp32 accumulation
+ * and online softmax, bf16 output.
+ * q: [B][H][N][D]; k, v: [B][H][kv_capacity][D]; o: [B][H][N][D].
+ * Errors: VAR_ERR_INVALID_ARG (null pointer, step out of range, kv_capacity < L),
+ * VAR_ERR_UNSUPPORTED (head_dim, alignment), VAR_ERR_CUDA (launch failure).
+ */
+VAR_API int var_attn_dense(const var_problem* p, int32_t step, const void* q, const void* k,
+                   const void* v, void* o, void* stream);
+
+/*
+ * Bytes of device workspace var_pivot_select needs for this step and channel
+ * count (0 on invalid arguments).
+ */
+VAR_API size_t var_pivot_workspace_bytes(const var_problem* p, int32_t step, int32_t channels);
+
+/*
+ * Pivot selection for cached token pruning ("FastVAR: Linear Visual
+ * Autoregressive Modeling via Cached Token Pruning", abstract: only pivotal
+ * tokens are forwarded; "ARVAR" Key Design 2: Top-K indices gather the tokens).
+ * Per batch element b, with m_b the mean of x[b] over the N grid tokens:
+ *   score[b,i] = ||x[b,i,:] - m_b||_2^2
+ * keeps the keep_k largest scores (equal scores: the lower flat index first)
+ * and writes their indices in ascending order.  The ranking is that of the
+ * fp64 evaluation (channel sums as a pairwise-halving tree): fp32 scores
+ * decide every token outside a certified error band; band tokens are
+ * re-scored in fp64 on the device.
+ * x: [B][N][channels] bf16, channels a positive multiple of 32, |x| < 2^20.
+ * idx: [B][keep_k] int32 (device).  scores: optional [B][N] fp32 (device) or NULL.
+ * workspace: device memory of var_pivot_workspace_bytes() bytes, 256-byte
+ * aligned; its contents on entry do not matter.
+ * Errors: VAR_ERR_INVALID_ARG (keep_k < 0 or > N, null pointers, channels),
+ * VAR_ERR_WORKSPACE, VAR_ERR_NUMERIC is reported through the device status
+ * word when an input exceeds the exactly-summed range.
+ */
+VAR_API int var_pivot_select(const var_problem* p, int32_t step, const void* x, int32_t channels,
+                     int32_t keep_k, int32_t* idx, float* scores, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/*
+ * Pruned attention: dense attention for the kept query rows only, against the
+ * full L-token cache ("FastVAR" abstract; "ARVAR" Key Design 2: only the
+ * gathered positions undergo attention).
+ *   O_c[b,h,j,:] = attention(Q[b,h,idx[b,j],:], K[b,h,:L], V[b,h,:L]),  j < keep_k
+ * q: [B][H][N][D]; idx: [B][keep_k] int32 device, each in [0, N);
+ * o_compact: [B][H][keep_k][D].  keep_k = 0 is a no-op.
+ * Errors: as var_attn_dense; indices are not checked on the device beyond
+ * clamping reads into the (b,h) query block.
+ */
+VAR_API int var_attn_pruned(const var_problem* p, int32_t step, const void* q, const void* k,
+                    const void* v, const int32_t* idx, int32_t keep_k, void* o_compact,
+                    void* stream);
+
+/*
+ * Structural reconstruction ("ARVAR" Key Design 3, Eq. (8)-(9)):
+ *   out = Scatter(Up(prev; s, s), idx, o_compact)
+ * Up is bilinear interpolation of the previous step's s' x s' output grid
+ * (s' = side[step-1], s = side[step]) with half-pixel centres and edge clamp;
+ * Scatter overwrites rows idx[b, j] with o_compact[b, h, j] (no blending).
+ * prev: [B][H][s'^2][D]; o_compact: [B][H][keep_k][D]; idx: [B][keep_k] strictly
+ * ascending, in [0, s^2); out: [B][H][s^2][D].  step >= 1.  keep_k = 0 gives
+ * the plain upsample; keep_k = N copies o_compact.
+ * Errors: VAR_ERR_INVALID_ARG (step 0, keep_k out of range, null pointers).
+ */
+VAR_API int var_restore_scatter(const var_problem* p, int32_t step, const void* prev,
+                        const void* o_compact, const int32_t* idx, int32_t keep_k, void* out,
+                        void* stream);
+
+/*
+ * Block mask for cross-scale local sparse attention (SparVAR abstract:
+ * attention sinks + cross-scale locality, evaluated block-wise).
+ * The query grid (side s_q = side[step], a multiple of qblock_side) is cut into
+ * qblock_side x qblock_side patches, numbered row-major.  For query block
+ * (by, bx) and every key scale of side s:
+ *   - s <= sink_max_side: every token of the scale is kept (the sink range,
+ *     the first sink_len cache tokens when those scales lead the schedule);
+ *   - otherwise the window of +-radius query blocks around (by, bx), clipped to
+ *     the grid, is rescaled into the key scale (lo*s/s_q rounded down,
+ *     hi*s/s_q rounded up) and every qblock_side x qblock_side key block of
+ *     that scale meeting it is kept.
+ * Entries are packed (scale << 24) | (u << 12) | v, u/v the key block row and
+ * column inside the scale, ascending within a row.
+ */
+typedef struct {
+    int32_t qblock_side;   /* query/key block side, e.g. 8 */
+    int32_t n_qblocks;     /* (side[step] / qblock_side)^2 */
+    int32_t sink_len;      /* tokens of the leading scales with side <= sink_max_side */
+    int32_t nnz;           /* entries[] length */
+    const int32_t* row_ptr;  /* device [n_qblocks + 1] */
+    const int32_t* entries;  /* device [nnz] */
+} var_block_mask;
+
+/*
+ * Build the block mask on the HOST.  row_ptr must hold n_qblocks + 1 ints and
+ * entries `entries_cap` ints (host memory).  Call once with entries = NULL to
+ * get *nnz_out (and *n_qblocks_out, *sink_len_out) for sizing.
+ * Errors: VAR_ERR_INVALID_ARG (sizes), VAR_ERR_UNSUPPORTED (side[step] not a
+ * multiple of qblock_side, sink scales not leading the schedule).
+ */
+VAR_API int var_block_mask_build(const var_problem* p, int32_t step, int32_t qblock_side,
+                         int32_t radius, int32_t sink_max_side, int32_t* row_ptr,
+                         int32_t* entries, int32_t entries_cap, int32_t* nnz_out,
+                         int32_t* n_qblocks_out, int32_t* sink_len_out);
+
+/*
+ * Block-sparse cross-scale attention: as var_attn_dense, but query i of block
+ * qb attends only to the sink range plus the key blocks listed for qb in
+ * `mask` (whose arrays are device copies of var_block_mask_build's output).
+ * q, o: [B][H][N][D]; k, v: [B][H][kv_capacity][D].
+ * Errors: as var_attn_dense, plus VAR_ERR_INVALID_ARG for a mask that does not
+ * match the step (block counts).
+ */
+VAR_API int var_attn_blocksparse(const var_problem* p, int32_t step, const void* q, const void* k,
+                         const void* v, const var_block_mask* mask, void* o, void* stream);
+
+/* floor(n * num / den) in exact integer arithmetic (the kept-query count). */
+VAR_API int32_t var_keep_count(int32_t n, int32_t num, int32_t den);
+
+/* A static, human-readable name for a var_status code. */
+VAR_API const char* var_status_string(int status);
+
+/*
+ * Read (and optionally clear) the device status word of the current device:
+ * VAR_OK, or the first VAR_ERR_TIMEOUT / VAR_ERR_NUMERIC a kernel recorded.
+ * Synchronises the device.  Returns VAR_OK or VAR_ERR_CUDA.
+ */
+VAR_API int var_device_status(int32_t* status_out, int32_t clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VARATTN_H */

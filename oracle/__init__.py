@@ -55,11 +55,18 @@ def lib():
         L.oracle_pivot_select.argtypes = [C.c_int, C.c_int, C.c_int, P, C.c_int, P, P]
         L.oracle_restore_scatter.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, P, P,
                                              P, C.c_int, P]
+        L.oracle_num_threads.restype = C.c_int
+        L.oracle_num_threads.argtypes = []
         for f in ("oracle_attention", "oracle_block_mask_rows", "oracle_pivot_mean",
                   "oracle_pivot_scores", "oracle_pivot_select", "oracle_restore_scatter"):
             getattr(L, f).restype = C.c_int
         _lib = L
     return _lib
+
+
+def num_threads() -> int:
+    """Threads the oracle's parallel loops use."""
+    return int(lib().oracle_num_threads())
 
 
 def _bits(t: torch.Tensor) -> np.ndarray:

@@ -43,8 +43,21 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define ORACLE_MAX_SCALES 32
+
+/* Threads the parallel loops below use (for reporting CPU-baseline timings). */
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
 
 static double bf16_to_f64(uint16_t h)
 {

@@ -1,0 +1,34 @@
+"""Shared helpers for the GPU parity tests."""
+import numpy as np
+import torch
+
+# Attention outputs on bf16 inputs: max-abs 2e-2 and mean-abs 2e-3 against the fp64 oracle.
+ATOL_MAX = 2e-2
+ATOL_MEAN = 2e-3
+
+
+def assert_close(got: torch.Tensor, ref: np.ndarray, what: str = "", max_abs=ATOL_MAX, mean_abs=ATOL_MEAN):
+    g = got.detach().float().cpu().double().numpy().reshape(ref.shape)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite output"
+    err = np.abs(g - ref)
+    assert err.max() <= max_abs, f"{what}: max abs err {err.max():.3e} > {max_abs}"
+    assert err.mean() <= mean_abs, f"{what}: mean abs err {err.mean():.3e} > {mean_abs}"
+    return float(err.max()), float(err.mean())
+
+
+def sample_rows(B, H, N, n, seed=0, extra=()):
+    """Flat query ids spread over (b, h) and the tile boundaries, plus the last row."""
+    g = np.random.default_rng(seed)
+    rows = set(int(r) for r in g.integers(0, B * H * N, size=n))
+    for bh in (0, B * H - 1):
+        for i in (0, 127, 128, 255, 256, N - 129, N - 2, N - 1):
+            if 0 <= i < N:
+                rows.add(bh * N + i)
+    rows.update(extra)
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def check_device_status():
+    import visual_autoregressive_next_var_b300 as V
+    st = V.var_device_status(clear=True)
+    assert st == 0, f"device status word: {st} ({V.var_status_string(st)})"

@@ -1,0 +1,152 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+declared entry point, rejects bad arguments before touching the device, and
+its host-built block mask equals the oracle's token-level rule exactly."""
+import ctypes as C
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import visual_autoregressive_next_var_b300 as V
+from var_synth import SCHEDULE_1024, SCHEDULE_2K, SCHEDULE_256
+
+
+def test_library_exports_every_declared_symbol():
+    names = V.header_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(V.lib(), n), n
+    for n in ("var_attn_dense", "var_attn_pruned", "var_attn_blocksparse", "var_pivot_select",
+              "var_restore_scatter"):
+        assert n in names
+
+
+def test_keep_count_and_status_strings():
+    assert V.var_keep_count(4096, 1, 5) == 819
+    assert V.var_keep_count(2304, 2, 5) == 921
+    assert V.var_keep_count(4096, 1, 1) == 4096
+    assert V.var_keep_count(7, 0, 3) == 0
+    assert V.var_keep_count(7, 4, 3) == -1
+    for s in range(7):
+        assert V.var_status_string(s) != "unknown status"
+    assert V.var_status_string(99) == "unknown status"
+
+
+def _fake(n=1 << 20):
+    # a host address never dereferenced: every call below must fail validation first
+    return C.c_void_p(0x10000)
+
+
+@pytest.mark.parametrize("head_dim,expect", [(96, V.VAR_ERR_UNSUPPORTED), (0, V.VAR_ERR_UNSUPPORTED)])
+def test_dense_rejects_head_dim(head_dim, expect):
+    p = V.problem(1, 2, head_dim, SCHEDULE_256)
+    assert V.lib().var_attn_dense(C.byref(p), 9, _fake(), _fake(), _fake(), _fake(), None) == expect
+
+
+def test_dense_rejects_bad_arguments():
+    L = V.lib()
+    p = V.problem(1, 2, 64, SCHEDULE_256)
+    f = _fake()
+    assert L.var_attn_dense(C.byref(p), 9, None, f, f, f, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_attn_dense(C.byref(p), 10, f, f, f, f, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_attn_dense(C.byref(p), -1, f, f, f, f, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_attn_dense(None, 0, f, f, f, f, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_attn_dense(C.byref(p), 9, C.c_void_p(0x10008), f, f, f, None) == V.VAR_ERR_UNSUPPORTED
+    small = V.problem(1, 2, 64, SCHEDULE_256, kv_capacity=679)
+    assert L.var_attn_dense(C.byref(small), 9, f, f, f, f, None) == V.VAR_ERR_INVALID_ARG
+    neg = V.problem(1, 2, 64, SCHEDULE_256, softmax_scale=-1.0)
+    assert L.var_attn_dense(C.byref(neg), 9, f, f, f, f, None) == V.VAR_ERR_INVALID_ARG
+
+
+def test_pruned_restore_pivot_reject_bad_arguments():
+    L = V.lib()
+    p = V.problem(2, 16, 128, SCHEDULE_1024)
+    f = _fake()
+    assert L.var_attn_pruned(C.byref(p), 12, f, f, f, f, 4097, f, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_attn_pruned(C.byref(p), 12, f, f, f, f, -1, f, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_attn_pruned(C.byref(p), 12, f, f, f, None, 5, f, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_attn_pruned(C.byref(p), 12, f, f, f, f, 0, f, None) == V.VAR_OK   # no-op
+    assert L.var_restore_scatter(C.byref(p), 0, f, f, f, 4, f, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_restore_scatter(C.byref(p), 12, f, None, None, 3, f, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_restore_scatter(C.byref(p), 12, f, f, f, 4097, f, None) == V.VAR_ERR_INVALID_ARG
+    ws = L.var_pivot_workspace_bytes(C.byref(p), 12, 2048)
+    assert ws > 0
+    assert L.var_pivot_workspace_bytes(C.byref(p), 12, 2047) == 0
+    assert L.var_pivot_select(C.byref(p), 12, f, 2048, 819, f, None, None, 0, None) == V.VAR_ERR_WORKSPACE
+    assert L.var_pivot_select(C.byref(p), 12, f, 2048, 819, f, None, f, ws - 1, None) == V.VAR_ERR_WORKSPACE
+    assert L.var_pivot_select(C.byref(p), 12, f, 2040, 819, f, None, f, ws, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_pivot_select(C.byref(p), 12, f, 2048, 4097, f, None, f, ws, None) == V.VAR_ERR_INVALID_ARG
+
+
+def _csr_to_token_mask(sides, step, qbs, row_ptr, entries, sink_len):
+    """Expand the library's block CSR into a [N, L] token mask."""
+    sq = sides[step]
+    nb = sq // qbs
+    offs = np.cumsum([0] + [s * s for s in sides[: step + 1]])
+    L = offs[-1]
+    out = np.zeros((sq * sq, L), dtype=bool)
+    for qb in range(nb * nb):
+        by, bx = divmod(qb, nb)
+        keys = np.zeros(L, dtype=bool)
+        keys[:sink_len] = True
+        for e in entries[row_ptr[qb]:row_ptr[qb + 1]]:
+            sc, u, w = e >> 24, (e >> 12) & 0xFFF, e & 0xFFF
+            s = sides[sc]
+            for r in range(u * qbs, min(s, u * qbs + qbs)):
+                c0, c1 = w * qbs, min(s, w * qbs + qbs)
+                keys[offs[sc] + r * s + c0: offs[sc] + r * s + c1] = True
+        for y in range(by * qbs, by * qbs + qbs):
+            out[y * sq + bx * qbs: y * sq + bx * qbs + qbs] = keys
+    return out
+
+
+@pytest.mark.parametrize("sides,qbs,radius,sink", [
+    ((1, 2, 4, 6, 8, 12, 16, 20, 24, 32), 8, 2, 16),
+    ((1, 2, 4, 8, 12, 16, 24, 32), 8, 1, 8),
+    ((1, 3, 5, 10, 15, 20), 5, 1, 5),
+    ((1, 2, 4, 6, 8, 12, 16), 4, 0, 4),
+])
+def test_block_mask_csr_equals_oracle_token_mask(sides, qbs, radius, sink):
+    step = len(sides) - 1
+    p = V.problem(1, 1, 64, sides)
+    row_ptr, entries, sink_len = V.var_block_mask_build(p, step, qbs, radius, sink)
+    assert sink_len == sum(s * s for s in sides if s <= sink)
+    got = _csr_to_token_mask(sides, step, qbs, row_ptr, entries, sink_len)
+    ref = oracle.block_mask_rows(oracle.mask_spec(sides, step, qbs, radius, sink), 0, sides[step] ** 2)
+    assert np.array_equal(got, ref.astype(bool))
+
+
+def test_block_mask_2k_statistics_and_rows():
+    p = V.problem(2, 16, 128, SCHEDULE_2K)
+    row_ptr, entries, sink_len = V.var_block_mask_build(p, 15, 8, 2, 16)
+    assert sink_len == 521 and row_ptr.shape == (257,) and len(entries) == 20164
+    assert np.all(np.diff(row_ptr) > 0)
+    for qb in range(256):
+        e = entries[row_ptr[qb]:row_ptr[qb + 1]]
+        assert np.all(np.diff(e) > 0)             # ascending, no duplicates
+    # spot-check whole rows of blocks against the oracle rule
+    sides = SCHEDULE_2K
+    m = oracle.mask_spec(sides, 15, 8, 2, 16)
+    offs = np.cumsum([0] + [s * s for s in sides])
+    for qb in (0, 17, 136, 255):
+        by, bx = divmod(qb, 16)
+        qi = (by * 8) * 128 + bx * 8
+        ref = oracle.block_mask_rows(m, qi, qi + 1)[0].astype(bool)
+        keys = np.zeros(offs[-1], dtype=bool)
+        keys[:sink_len] = True
+        for e in entries[row_ptr[qb]:row_ptr[qb + 1]]:
+            sc, u, w = e >> 24, (e >> 12) & 0xFFF, e & 0xFFF
+            s = sides[sc]
+            for r in range(u * 8, min(s, u * 8 + 8)):
+                keys[offs[sc] + r * s + w * 8: offs[sc] + r * s + min(s, w * 8 + 8)] = True
+        assert np.array_equal(keys, ref)
+
+
+def test_block_mask_rejects_bad_shapes():
+    p = V.problem(1, 1, 64, (1, 2, 4, 6, 8, 12, 16, 20))
+    with pytest.raises(V.VarError):
+        V.var_block_mask_build(p, 7, 8, 2, 16)      # 20 is not a multiple of 8
+    q = V.problem(1, 1, 64, (1, 32, 4, 64))
+    with pytest.raises(V.VarError):
+        V.var_block_mask_build(q, 3, 8, 1, 4)       # a sink scale after a non-sink one

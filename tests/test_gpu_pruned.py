@@ -1,0 +1,188 @@
+"""GPU parity: cached token pruning -- pivot selection (bit-exact indices),
+pruned attention, restore + scatter, and the chained 1024px pruned steps."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import visual_autoregressive_next_var_b300 as V
+from var_synth import WORKLOADS, cache_len, make_inputs, randn_bf16
+from tests._util import assert_close, check_device_status, sample_rows
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def gpu_pivot(p, step, x, keep_k, want_scores=False):
+    B, N, Cc = x.shape
+    ws = torch.empty(V.var_pivot_workspace_bytes(p, step, Cc), dtype=torch.uint8, device=DEV)
+    idx = torch.full((B, max(keep_k, 1)), -1, dtype=torch.int32, device=DEV)
+    sc = torch.empty((B, N), dtype=torch.float32, device=DEV) if want_scores else None
+    V.var_pivot_select(p, step, x.to(DEV), keep_k, idx, ws, sc)
+    torch.cuda.synchronize()
+    return idx[:, :keep_k].cpu().numpy(), (sc.cpu().numpy() if want_scores else None)
+
+
+# ---------------------------------------------------------------- pivot selection
+
+@pytest.mark.parametrize("step,num,den", [(11, 2, 5), (12, 1, 5)])
+def test_pivot_workload_bit_exact(step, num, den):
+    w = WORKLOADS["pruned_1024px"]
+    inp = make_inputs(w)
+    x = inp.x[step]
+    B, N, Cc = x.shape
+    K = V.var_keep_count(N, num, den)
+    p = V.problem(w.batch, w.heads, w.head_dim, w.sides)
+    got, sc = gpu_pivot(p, step, x, K, want_scores=True)
+    ref, ref_sc = oracle.pivot_select(x, K)
+    assert np.array_equal(got, ref)
+    assert np.max(np.abs(sc - ref_sc) / ref_sc) < 1e-4
+    check_device_status()
+
+
+@pytest.mark.parametrize("N,Cc,K,seed", [(64, 32, 10, 0), (100, 64, 99, 1), (169, 256, 1, 2),
+                                          (256, 2048, 128, 3), (400, 96, 200, 4), (1024, 512, 1024, 5)])
+def test_pivot_random_shapes(N, Cc, K, seed):
+    s = int(round(N ** 0.5))
+    p = V.problem(2, 1, 64, (1, s))
+    x = randn_bf16((2, N, Cc), 50 + seed)
+    got, _ = gpu_pivot(p, 1, x, K)
+    ref, _ = oracle.pivot_select(x, K)
+    assert np.array_equal(got, ref)
+    check_device_status()
+
+
+def test_pivot_ties_and_degenerate_grids():
+    p = V.problem(2, 1, 64, (1, 16))
+    const = torch.full((2, 256, 64), 0.375).to(torch.bfloat16)
+    got, _ = gpu_pivot(p, 1, const, 37)
+    assert np.array_equal(got, np.tile(np.arange(37), (2, 1)))          # all tied: lowest indices
+    x = randn_bf16((2, 256, 64), 60)
+    x[:, 200] = 4.0
+    x[:, 17] = 4.0                                                      # identical extreme rows
+    got, _ = gpu_pivot(p, 1, x, 1)
+    assert np.array_equal(got, [[17], [17]])
+    got2, _ = gpu_pivot(p, 1, x, 2)
+    assert np.array_equal(got2, [[17, 200], [17, 200]])
+    dup = randn_bf16((2, 16, 64), 61).repeat(1, 16, 1)                  # 16 copies of 16 rows
+    got3, _ = gpu_pivot(p, 1, dup, 40)
+    ref3, _ = oracle.pivot_select(dup, 40)
+    assert np.array_equal(got3, ref3)
+    got4, _ = gpu_pivot(p, 1, x, 256)
+    assert np.array_equal(got4, np.tile(np.arange(256), (2, 1)))
+    got0, _ = gpu_pivot(p, 1, x, 0)
+    assert got0.shape == (2, 0)
+    check_device_status()
+
+
+# ---------------------------------------------------------------- pruned attention
+
+@pytest.mark.parametrize("K", [1, 130, 819, 4096])
+def test_pruned_attention_sampled(K):
+    w = WORKLOADS["pruned_1024px"]
+    inp = make_inputs(w, steps=(12,))
+    step = 12
+    q = inp.q[step]
+    B, H, N, D = q.shape
+    L = cache_len(w.sides, step)
+    g = torch.Generator().manual_seed(K)
+    idx = torch.stack([torch.sort(torch.randperm(N, generator=g)[:K])[0] for _ in range(B)]).to(torch.int32)
+    p = V.problem(B, H, D, w.sides)
+    oc = torch.empty((B, H, K, D), dtype=torch.bfloat16, device=DEV)
+    V.var_attn_pruned(p, step, q.to(DEV), inp.k.to(DEV), inp.v.to(DEV), idx.to(DEV), K, oc)
+    torch.cuda.synchronize()
+    # compact row (b, h, j) is query row (b, h, idx[b, j])
+    crow = sample_rows(B, H, K, 96, seed=K)
+    bh, j = crow // K, crow % K
+    b = bh // H
+    qrows = bh * N + idx.numpy()[b, j]
+    ref = oracle.attention(q, inp.k, inp.v, L, rows=qrows)
+    got = oc.reshape(-1, D)[torch.as_tensor(crow, device=DEV)]
+    assert_close(got, ref, f"pruned K={K}")
+    check_device_status()
+
+
+def test_pruned_keep_all_equals_dense():
+    sides, D, B, H = (1, 2, 4, 6, 9, 14, 20), 128, 2, 2
+    step, N, L = 6, 400, cache_len(sides, 6)
+    q = randn_bf16((B, H, N, D), 70)
+    k = randn_bf16((B, H, L, D), 71)
+    v = randn_bf16((B, H, L, D), 72)
+    p = V.problem(B, H, D, sides)
+    idx = torch.arange(N, dtype=torch.int32).repeat(B, 1).to(DEV)
+    oc = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=DEV)
+    od = torch.empty_like(oc)
+    V.var_attn_pruned(p, step, q.to(DEV), k.to(DEV), v.to(DEV), idx, N, oc)
+    V.var_attn_dense(p, step, q.to(DEV), k.to(DEV), v.to(DEV), od)
+    torch.cuda.synchronize()
+    assert torch.equal(oc, od)
+    check_device_status()
+
+
+# ---------------------------------------------------------------- restore + scatter
+
+@pytest.mark.parametrize("sp,s,K,D", [(48, 64, 819, 128), (40, 48, 921, 128), (13, 16, 0, 64),
+                                      (13, 16, 256, 64), (5, 6, 7, 128), (64, 64, 100, 128)])
+def test_restore_scatter(sp, s, K, D):
+    B, H = 2, 3
+    sides = (1, sp, s) if sp != s else (1, s, s)
+    p = V.problem(B, H, D, sides)
+    prev = randn_bf16((B, H, sp * sp, D), 80 + s)
+    oc = randn_bf16((B, H, max(K, 1), D), 81 + s)[:, :, :K].contiguous()
+    g = torch.Generator().manual_seed(K + s)
+    idx = torch.stack([torch.sort(torch.randperm(s * s, generator=g)[:K])[0] for _ in range(B)]).to(torch.int32)
+    out = torch.empty((B, H, s * s, D), dtype=torch.bfloat16, device=DEV)
+    V.var_restore_scatter(p, 2, prev.to(DEV), oc.to(DEV) if K else None, idx.to(DEV) if K else None, K, out)
+    torch.cuda.synchronize()
+    ref = oracle.restore_scatter(prev, oc, idx.numpy(), s)
+    assert_close(out, ref, f"restore {sp}->{s} K={K}")
+    outc = out.cpu()
+    for b in range(B):
+        assert torch.equal(outc[b][:, idx[b].long()], oc[b])          # kept rows: exact copies
+    check_device_status()
+
+
+# ---------------------------------------------------------------- the chained pruned steps
+
+def test_pruned_chain_1024px():
+    """40x40 dense -> 48x48 pruned (r=0.4) + restore -> 64x64 pruned (r=0.2) + restore.
+    The oracle runs the same chain, rounding each stage's output to bf16 as the
+    GPU stores it; the pivot indices are compared bit for bit at both steps."""
+    w = WORKLOADS["pruned_1024px"]
+    inp = make_inputs(w)
+    B, H, D = w.batch, w.heads, w.head_dim
+    p = V.problem(B, H, D, w.sides, kv_capacity=w.n_tokens)   # one cache for every step
+    k, v = inp.k.to(DEV), inp.v.to(DEV)
+    # step 10: dense 40x40
+    q10 = inp.q[10]
+    o10 = torch.empty_like(q10, device=DEV)
+    V.var_attn_dense(p, 10, q10.to(DEV), k, v, o10)
+    torch.cuda.synchronize()
+    rows10 = sample_rows(B, H, 1600, 48, seed=10)
+    assert_close(o10.reshape(-1, D)[torch.as_tensor(rows10, device=DEV)],
+                 oracle.attention(q10, inp.k, inp.v, cache_len(w.sides, 10), rows=rows10), "chain step 10")
+    prev = o10
+    for step, num, den in ((11, 2, 5), (12, 1, 5)):
+        x = inp.x[step]
+        N = x.shape[1]
+        K = V.var_keep_count(N, num, den)
+        idx_g, _ = gpu_pivot(p, step, x, K)
+        idx_ref, _ = oracle.pivot_select(x, K)
+        assert np.array_equal(idx_g, idx_ref), f"pivot indices differ at step {step}"
+        idx_d = torch.as_tensor(idx_g, device=DEV)
+        oc = torch.empty((B, H, K, D), dtype=torch.bfloat16, device=DEV)
+        V.var_attn_pruned(p, step, inp.q[step].to(DEV), k, v, idx_d, K, oc)
+        out = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=DEV)
+        V.var_restore_scatter(p, step, prev, oc, idx_d, K, out)
+        torch.cuda.synchronize()
+        # oracle restore on the GPU's own bf16 inputs of this stage
+        ref = oracle.restore_scatter(prev.cpu(), oc.cpu(), idx_g, w.sides[step])
+        assert_close(out, ref, f"chain restore step {step}")
+        # sampled pruned rows against the oracle
+        crow = sample_rows(B, H, K, 32, seed=step)
+        bh, j = crow // K, crow % K
+        qrows = bh * N + idx_g[bh // H, j]
+        ref_rows = oracle.attention(inp.q[step], inp.k, inp.v, cache_len(w.sides, step), rows=qrows)
+        assert_close(oc.reshape(-1, D)[torch.as_tensor(crow, device=DEV)], ref_rows, f"chain pruned {step}")
+        prev = out
+    check_device_status()

@@ -1,0 +1,203 @@
+"""Python binding of libvarattn (include/varattn.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls and does no
+arithmetic of its own: tensors are passed as device pointers, the stream is
+torch's current CUDA stream unless one is given, and a non-zero status raises
+``VarError``.  PyTorch is used only to own device memory and streams.
+
+Importing this module loads the shared library and fails loudly if it is
+missing; run ``python -m visual_autoregressive_next_var_b300.build`` (or
+``__graft_entry__.build()``) first.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+from typing import Optional, Sequence, Tuple
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libvarattn.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "varattn.h")
+MAX_SCALES = 32
+
+VAR_OK = 0
+VAR_ERR_INVALID_ARG = 1
+VAR_ERR_UNSUPPORTED = 2
+VAR_ERR_CUDA = 3
+VAR_ERR_TIMEOUT = 4
+VAR_ERR_NUMERIC = 5
+VAR_ERR_WORKSPACE = 6
+
+
+class VarError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {status} ({var_status_string(status)})")
+        self.status = status
+
+
+class var_problem(C.Structure):
+    _fields_ = [("batch", C.c_int32), ("heads", C.c_int32), ("head_dim", C.c_int32),
+                ("n_scales", C.c_int32), ("side", C.c_int32 * MAX_SCALES),
+                ("kv_capacity", C.c_int32), ("softmax_scale", C.c_float)]
+
+
+class var_block_mask(C.Structure):
+    _fields_ = [("qblock_side", C.c_int32), ("n_qblocks", C.c_int32), ("sink_len", C.c_int32),
+                ("nnz", C.c_int32), ("row_ptr", C.c_void_p), ("entries", C.c_void_p)]
+
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build the CUDA library first "
+                      "(python -m visual_autoregressive_next_var_b300.build)")
+_lib = C.CDLL(LIB_PATH)
+
+_P = C.c_void_p
+_PROB = C.POINTER(var_problem)
+_SIGS = {
+    "var_attn_dense": (C.c_int, [_PROB, C.c_int32, _P, _P, _P, _P, _P]),
+    "var_pivot_workspace_bytes": (C.c_size_t, [_PROB, C.c_int32, C.c_int32]),
+    "var_pivot_select": (C.c_int, [_PROB, C.c_int32, _P, C.c_int32, C.c_int32, _P, _P, _P,
+                                   C.c_size_t, _P]),
+    "var_attn_pruned": (C.c_int, [_PROB, C.c_int32, _P, _P, _P, _P, C.c_int32, _P, _P]),
+    "var_restore_scatter": (C.c_int, [_PROB, C.c_int32, _P, _P, _P, C.c_int32, _P, _P]),
+    "var_block_mask_build": (C.c_int, [_PROB, C.c_int32, C.c_int32, C.c_int32, C.c_int32, _P, _P,
+                                       C.c_int32, _P, _P, _P]),
+    "var_attn_blocksparse": (C.c_int, [_PROB, C.c_int32, _P, _P, _P,
+                                       C.POINTER(var_block_mask), _P, _P]),
+    "var_keep_count": (C.c_int32, [C.c_int32, C.c_int32, C.c_int32]),
+    "var_status_string": (C.c_char_p, [C.c_int]),
+    "var_device_status": (C.c_int, [_P, C.c_int32]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+
+def header_functions() -> Sequence[str]:
+    """Names of the functions include/varattn.h declares."""
+    text = open(HEADER_PATH).read()
+    return re.findall(r"^\s*VAR_API\s+(?:int|int32_t|size_t|const char\*)\s+(var_\w+)\s*\(", text, re.M)
+
+
+def lib() -> C.CDLL:
+    return _lib
+
+
+def problem(batch: int, heads: int, head_dim: int, sides: Sequence[int], kv_capacity: int = 0,
+            softmax_scale: float = 0.0) -> var_problem:
+    p = var_problem()
+    p.batch, p.heads, p.head_dim = batch, heads, head_dim
+    p.n_scales = len(sides)
+    for i, s in enumerate(sides):
+        p.side[i] = s
+    p.kv_capacity = kv_capacity
+    p.softmax_scale = softmax_scale
+    return p
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> C.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(name: str, rc: int) -> None:
+    if rc != VAR_OK:
+        raise VarError(name, rc)
+
+
+def var_status_string(status: int) -> str:
+    return _lib.var_status_string(status).decode()
+
+
+def var_keep_count(n: int, num: int, den: int) -> int:
+    return _lib.var_keep_count(n, num, den)
+
+
+def var_device_status(clear: bool = True) -> int:
+    out = C.c_int32(0)
+    _check("var_device_status", _lib.var_device_status(C.byref(out), 1 if clear else 0))
+    return out.value
+
+
+def var_attn_dense(p: var_problem, step: int, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                   o: torch.Tensor, stream=None) -> None:
+    _check("var_attn_dense", _lib.var_attn_dense(C.byref(p), step, _ptr(q), _ptr(k), _ptr(v),
+                                                 _ptr(o), _stream(stream)))
+
+
+def var_pivot_workspace_bytes(p: var_problem, step: int, channels: int) -> int:
+    return _lib.var_pivot_workspace_bytes(C.byref(p), step, channels)
+
+
+def var_pivot_select(p: var_problem, step: int, x: torch.Tensor, keep_k: int, idx: torch.Tensor,
+                     workspace: torch.Tensor, scores: Optional[torch.Tensor] = None,
+                     stream=None) -> None:
+    channels = x.shape[-1]
+    _check("var_pivot_select",
+           _lib.var_pivot_select(C.byref(p), step, _ptr(x), channels, keep_k, _ptr(idx),
+                                 _ptr(scores), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _stream(stream)))
+
+
+def var_attn_pruned(p: var_problem, step: int, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                    idx: torch.Tensor, keep_k: int, o_compact: torch.Tensor, stream=None) -> None:
+    _check("var_attn_pruned", _lib.var_attn_pruned(C.byref(p), step, _ptr(q), _ptr(k), _ptr(v),
+                                                   _ptr(idx), keep_k, _ptr(o_compact),
+                                                   _stream(stream)))
+
+
+def var_restore_scatter(p: var_problem, step: int, prev: torch.Tensor, o_compact: Optional[torch.Tensor],
+                        idx: Optional[torch.Tensor], keep_k: int, out: torch.Tensor,
+                        stream=None) -> None:
+    _check("var_restore_scatter",
+           _lib.var_restore_scatter(C.byref(p), step, _ptr(prev), _ptr(o_compact), _ptr(idx), keep_k,
+                                    _ptr(out), _stream(stream)))
+
+
+def var_block_mask_build(p: var_problem, step: int, qblock_side: int, radius: int,
+                         sink_max_side: int) -> Tuple[np.ndarray, np.ndarray, int]:
+    """Host call: returns (row_ptr int32 [n_qblocks+1], entries int32 [nnz], sink_len)."""
+    nnz, nqb, sink = C.c_int32(), C.c_int32(), C.c_int32()
+    _check("var_block_mask_build",
+           _lib.var_block_mask_build(C.byref(p), step, qblock_side, radius, sink_max_side, None, None,
+                                     0, C.byref(nnz), C.byref(nqb), C.byref(sink)))
+    row_ptr = np.zeros(nqb.value + 1, dtype=np.int32)
+    entries = np.zeros(max(1, nnz.value), dtype=np.int32)
+    _check("var_block_mask_build",
+           _lib.var_block_mask_build(C.byref(p), step, qblock_side, radius, sink_max_side,
+                                     row_ptr.ctypes.data_as(C.c_void_p),
+                                     entries.ctypes.data_as(C.c_void_p), entries.size,
+                                     C.byref(nnz), C.byref(nqb), C.byref(sink)))
+    return row_ptr, entries[: nnz.value], sink.value
+
+
+def block_mask_struct(qblock_side: int, row_ptr: torch.Tensor, entries: torch.Tensor,
+                      sink_len: int) -> var_block_mask:
+    """var_block_mask over device copies of var_block_mask_build's arrays."""
+    m = var_block_mask()
+    m.qblock_side = qblock_side
+    m.n_qblocks = row_ptr.numel() - 1
+    m.sink_len = sink_len
+    m.nnz = entries.numel()
+    m.row_ptr = row_ptr.data_ptr()
+    m.entries = entries.data_ptr()
+    return m
+
+
+def var_attn_blocksparse(p: var_problem, step: int, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                         mask: var_block_mask, o: torch.Tensor, stream=None) -> None:
+    _check("var_attn_blocksparse",
+           _lib.var_attn_blocksparse(C.byref(p), step, _ptr(q), _ptr(k), _ptr(v), C.byref(mask),
+                                     _ptr(o), _stream(stream)))

@@ -1,0 +1,281 @@
+// The C ABI of include/varattn.h: argument checks, geometry, dispatch.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+
+namespace varattn {
+
+// One status word per device that loads this library.  Kernels record the first
+// fault they detect (CAS from 0); var_device_status() reads and clears it.
+static __device__ int32_t g_status_word;
+
+static std::mutex g_mu;
+
+int32_t* device_status_ptr()
+{
+    static int32_t* cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!cache[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        cache[dev] = static_cast<int32_t*>(p);
+    }
+    return cache[dev];
+}
+
+int encode_tmap_bf16(CUtensorMap* out, const void* base, int rank, const uint64_t* dims,
+                     const uint64_t* strides_bytes, const uint32_t* box)
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!fn) {
+            void* p = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                                 &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || !p)
+                return VAR_ERR_CUDA;
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        }
+    }
+    cuuint64_t d[5];
+    cuuint64_t s[4];
+    cuuint32_t b[5];
+    cuuint32_t e[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        e[i] = 1;
+        if (i + 1 < rank) s[i] = strides_bytes[i];
+    }
+    const CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+                          const_cast<void*>(base), d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? VAR_OK : VAR_ERR_CUDA;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Validate the problem and resolve the geometry of `step`.
+static int resolve(const var_problem* p, int32_t step, StepGeom* g)
+{
+    if (!p) return VAR_ERR_INVALID_ARG;
+    if (p->batch <= 0 || p->heads <= 0 || p->n_scales <= 0 || p->n_scales > VAR_MAX_SCALES)
+        return VAR_ERR_INVALID_ARG;
+    if (step < 0 || step >= p->n_scales) return VAR_ERR_INVALID_ARG;
+    if (p->head_dim != 64 && p->head_dim != 128) return VAR_ERR_UNSUPPORTED;
+    long long L = 0;
+    for (int i = 0; i <= step; ++i) {
+        if (p->side[i] <= 0 || p->side[i] > 4096) return VAR_ERR_INVALID_ARG;
+        L += static_cast<long long>(p->side[i]) * p->side[i];
+    }
+    if (L > (1ll << 30)) return VAR_ERR_UNSUPPORTED;
+    const long long cap = p->kv_capacity == 0 ? L : p->kv_capacity;
+    if (cap < L) return VAR_ERR_INVALID_ARG;
+    if (static_cast<long long>(p->batch) * p->heads > 65535ll * 64) return VAR_ERR_UNSUPPORTED;
+    if (!(p->softmax_scale >= 0.f) || !std::isfinite(p->softmax_scale)) return VAR_ERR_INVALID_ARG;
+    g->B = p->batch;
+    g->H = p->heads;
+    g->D = p->head_dim;
+    g->side = p->side[step];
+    g->N = g->side * g->side;
+    g->L = static_cast<int>(L);
+    g->cap = static_cast<int>(cap);
+    g->scale = p->softmax_scale == 0.f ? 1.0f / std::sqrt(static_cast<float>(p->head_dim))
+                                       : p->softmax_scale;
+    return VAR_OK;
+}
+
+}  // namespace varattn
+
+using namespace varattn;
+
+extern "C" {
+
+int var_attn_dense(const var_problem* p, int32_t step, const void* q, const void* k, const void* v,
+                   void* o, void* stream)
+{
+    StepGeom g;
+    if (int rc = resolve(p, step, &g)) return rc;
+    if (!q || !k || !v || !o) return VAR_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return VAR_ERR_UNSUPPORTED;
+    return launch_attn_dense(g, q, k, v, o, static_cast<cudaStream_t>(stream));
+}
+
+size_t var_pivot_workspace_bytes(const var_problem* p, int32_t step, int32_t channels)
+{
+    StepGeom g;
+    if (resolve(p, step, &g) != VAR_OK || channels <= 0 || channels % 32 != 0) return 0;
+    return pivot_workspace_bytes(g.B, g.N, channels);
+}
+
+int var_pivot_select(const var_problem* p, int32_t step, const void* x, int32_t channels,
+                     int32_t keep_k, int32_t* idx, float* scores, void* workspace,
+                     size_t workspace_bytes, void* stream)
+{
+    StepGeom g;
+    if (int rc = resolve(p, step, &g)) return rc;
+    if (!x || channels <= 0 || channels % 32 != 0 || channels > 16384) return VAR_ERR_INVALID_ARG;
+    if (keep_k < 0 || keep_k > g.N) return VAR_ERR_INVALID_ARG;
+    if (keep_k > 0 && !idx) return VAR_ERR_INVALID_ARG;
+    if (g.N > 16384) return VAR_ERR_UNSUPPORTED;
+    if (!aligned16(x)) return VAR_ERR_UNSUPPORTED;
+    const size_t need = pivot_workspace_bytes(g.B, g.N, channels);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return VAR_ERR_WORKSPACE;
+    return launch_pivot_select(g.B, g.N, channels, x, keep_k, idx, scores, workspace,
+                               workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int var_attn_pruned(const var_problem* p, int32_t step, const void* q, const void* k, const void* v,
+                    const int32_t* idx, int32_t keep_k, void* o_compact, void* stream)
+{
+    StepGeom g;
+    if (int rc = resolve(p, step, &g)) return rc;
+    if (keep_k < 0 || keep_k > g.N) return VAR_ERR_INVALID_ARG;
+    if (keep_k == 0) return VAR_OK;
+    if (!q || !k || !v || !idx || !o_compact) return VAR_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_compact))
+        return VAR_ERR_UNSUPPORTED;
+    return launch_attn_pruned(g, q, k, v, idx, keep_k, o_compact, static_cast<cudaStream_t>(stream));
+}
+
+int var_restore_scatter(const var_problem* p, int32_t step, const void* prev, const void* o_compact,
+                        const int32_t* idx, int32_t keep_k, void* out, void* stream)
+{
+    StepGeom g;
+    if (int rc = resolve(p, step, &g)) return rc;
+    if (step < 1) return VAR_ERR_INVALID_ARG;
+    if (keep_k < 0 || keep_k > g.N) return VAR_ERR_INVALID_ARG;
+    if (!prev || !out || (keep_k > 0 && (!o_compact || !idx))) return VAR_ERR_INVALID_ARG;
+    if (!aligned16(prev) || !aligned16(out) || (keep_k > 0 && !aligned16(o_compact)))
+        return VAR_ERR_UNSUPPORTED;
+    return launch_restore_scatter(g.B, g.H, g.D, p->side[step - 1], g.side, prev, o_compact, idx,
+                                  keep_k, out, static_cast<cudaStream_t>(stream));
+}
+
+int var_block_mask_build(const var_problem* p, int32_t step, int32_t qblock_side, int32_t radius,
+                         int32_t sink_max_side, int32_t* row_ptr, int32_t* entries,
+                         int32_t entries_cap, int32_t* nnz_out, int32_t* n_qblocks_out,
+                         int32_t* sink_len_out)
+{
+    StepGeom g;
+    if (int rc = resolve(p, step, &g)) return rc;
+    if (qblock_side <= 0 || qblock_side > 64 || radius < 0 || sink_max_side < 0)
+        return VAR_ERR_INVALID_ARG;
+    const int sq = g.side;
+    if (sq % qblock_side != 0) return VAR_ERR_UNSUPPORTED;
+    // The sink scales must lead the schedule so that they form one flat prefix.
+    int sink_len = 0;
+    bool in_prefix = true;
+    for (int sc = 0; sc <= step; ++sc) {
+        const int s = p->side[sc];
+        if (s <= sink_max_side) {
+            if (!in_prefix) return VAR_ERR_UNSUPPORTED;
+            sink_len += s * s;
+        } else {
+            in_prefix = false;
+            if ((s + qblock_side - 1) / qblock_side > 4095) return VAR_ERR_UNSUPPORTED;
+        }
+    }
+    const int nb = sq / qblock_side;
+    const int n_qb = nb * nb;
+    // Per axis and per key scale: the range of kept key blocks [u0, u1) for query
+    // block coordinate qb.  The window of +-radius query blocks is clipped to the
+    // grid, mapped into the key scale (low end rounded down, high end up), and
+    // widened to that scale's blocks.
+    auto block_range = [&](int qb, int s, int* u0, int* u1) {
+        const long long lo = std::max(0ll, static_cast<long long>(qblock_side) * (qb - radius));
+        const long long hi = std::min(static_cast<long long>(sq),
+                                      static_cast<long long>(qblock_side) * (qb + radius + 1));
+        const long long lo_s = lo * s / sq;
+        const long long hi_s = (hi * s + sq - 1) / sq;
+        *u0 = static_cast<int>(lo_s / qblock_side);
+        *u1 = static_cast<int>((hi_s + qblock_side - 1) / qblock_side);
+    };
+    long long nnz = 0;
+    for (int qb = 0; qb < n_qb; ++qb) {
+        const int by = qb / nb, bx = qb % nb;
+        if (row_ptr) row_ptr[qb] = static_cast<int32_t>(nnz);
+        for (int sc = 0; sc <= step; ++sc) {
+            const int s = p->side[sc];
+            if (s <= sink_max_side) continue;
+            int uy0, uy1, ux0, ux1;
+            block_range(by, s, &uy0, &uy1);
+            block_range(bx, s, &ux0, &ux1);
+            for (int u = uy0; u < uy1; ++u)
+                for (int w = ux0; w < ux1; ++w) {
+                    if (entries) {
+                        if (nnz >= entries_cap) return VAR_ERR_INVALID_ARG;
+                        entries[nnz] = (sc << 24) | (u << 12) | w;
+                    }
+                    ++nnz;
+                }
+        }
+    }
+    if (nnz > 0x7fffffffll) return VAR_ERR_UNSUPPORTED;
+    if (row_ptr) row_ptr[n_qb] = static_cast<int32_t>(nnz);
+    if (nnz_out) *nnz_out = static_cast<int32_t>(nnz);
+    if (n_qblocks_out) *n_qblocks_out = n_qb;
+    if (sink_len_out) *sink_len_out = sink_len;
+    return VAR_OK;
+}
+
+int var_attn_blocksparse(const var_problem* p, int32_t step, const void* q, const void* k,
+                         const void* v, const var_block_mask* mask, void* o, void* stream)
+{
+    StepGeom g;
+    if (int rc = resolve(p, step, &g)) return rc;
+    if (!q || !k || !v || !o || !mask || !mask->row_ptr || !mask->entries) return VAR_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return VAR_ERR_UNSUPPORTED;
+    if (mask->qblock_side <= 0 || g.side % mask->qblock_side != 0) return VAR_ERR_INVALID_ARG;
+    const int nb = g.side / mask->qblock_side;
+    if (mask->n_qblocks != nb * nb || mask->sink_len < 0 || mask->sink_len > g.L || mask->nnz < 0)
+        return VAR_ERR_INVALID_ARG;
+    return launch_attn_blocksparse(g, p->side, p->n_scales, step, q, k, v, mask, o,
+                                   static_cast<cudaStream_t>(stream));
+}
+
+int32_t var_keep_count(int32_t n, int32_t num, int32_t den)
+{
+    if (n < 0 || num < 0 || den <= 0 || num > den) return -1;
+    return static_cast<int32_t>(static_cast<int64_t>(n) * num / den);
+}
+
+const char* var_status_string(int status)
+{
+    switch (status) {
+    case VAR_OK: return "ok";
+    case VAR_ERR_INVALID_ARG: return "invalid argument";
+    case VAR_ERR_UNSUPPORTED: return "unsupported configuration";
+    case VAR_ERR_CUDA: return "CUDA runtime error";
+    case VAR_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case VAR_ERR_NUMERIC: return "input outside the exactly handled numeric range";
+    case VAR_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+    }
+}
+
+int var_device_status(int32_t* status_out, int32_t clear)
+{
+    int32_t* p = device_status_ptr();
+    if (!p || !status_out) return VAR_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return VAR_ERR_CUDA;
+    int32_t v = 0;
+    if (cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return VAR_ERR_CUDA;
+    *status_out = v;
+    if (clear && v != 0) {
+        const int32_t z = 0;
+        if (cudaMemcpy(p, &z, sizeof z, cudaMemcpyHostToDevice) != cudaSuccess) return VAR_ERR_CUDA;
+    }
+    return VAR_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,47 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "../../include/varattn.h"
+
+namespace varattn {
+
+// Resolved problem geometry for one step.
+struct StepGeom {
+    int B, H, D;
+    int side;        // s = side[step]
+    int N;           // s*s queries
+    int L;           // cached tokens of scales 0..step
+    int cap;         // rows per (b,h) in K/V
+    float scale;     // softmax scale
+};
+
+// Device address of this library's status word on the current device (0 on error).
+int32_t* device_status_ptr();
+
+// 3-D / 4-D bf16 tensor maps with 128-byte swizzle, box inner extent 64 elements.
+// dims/strides as cuTensorMapEncodeTiled takes them (strides in bytes, rank-1 of them).
+int encode_tmap_bf16(CUtensorMap* out, const void* base, int rank, const uint64_t* dims,
+                     const uint64_t* strides_bytes, const uint32_t* box);
+
+int launch_attn_dense(const StepGeom& g, const void* q, const void* k, const void* v, void* o,
+                      cudaStream_t st);
+int launch_attn_pruned(const StepGeom& g, const void* q, const void* k, const void* v,
+                       const int32_t* idx, int keep_k, void* o, cudaStream_t st);
+int launch_attn_blocksparse(const StepGeom& g, const int32_t* sides, int n_scales, int step,
+                            const void* q, const void* k, const void* v,
+                            const var_block_mask* mask, void* o, cudaStream_t st);
+size_t pivot_workspace_bytes(int B, int N, int C);
+int launch_pivot_select(int B, int N, int C, const void* x, int keep_k, int32_t* idx,
+                        float* scores, void* ws, size_t ws_bytes, cudaStream_t st);
+int launch_restore_scatter(int B, int H, int D, int sp, int s, const void* prev, const void* oc,
+                           const int32_t* idx, int keep_k, void* out, cudaStream_t st);
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? VAR_OK : VAR_ERR_CUDA; }
+
+}  // namespace varattn
