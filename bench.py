@@ -104,12 +104,15 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, enabled: bool = True):
         self.gpu = gpu_index
+        self.enabled = enabled
         self.proc = None
         self.file = None
 
     def __enter__(self):
+        if not self.enabled:
+            return self
         try:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
@@ -130,6 +133,8 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        if not self.enabled:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["not sampled (--no-clocks)"]}
         if self.proc is None or self.file is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.file.flush()
@@ -166,25 +171,34 @@ def time_loop(fn, steps: int, stream) -> float:
 
 # ----------------------------------------------------------------------------- CPU oracle arm
 
-def oracle_sample(w, inp, step, budget_s: float):
-    """Time the oracle on a bounded sample of query rows of `step`.
-    Returns (TFLOP/s, seconds, rows, threads)."""
+def oracle_calibrate(w, inp, step, budget_s: float):
+    """Number of query rows of `step` the oracle computes in about budget_s."""
     import oracle
     q = inp.q[step]
     B, H, N, D = q.shape
     L = cache_len(w.sides, step)
-    per_row = 4.0 * L * D
-    rng = np.random.default_rng(0)
-    n = 16
     oracle.attention(q, inp.k, inp.v, L, rows=np.arange(2))        # load + warm
+    n = 8
     while True:
-        rows = np.sort(rng.choice(B * H * N, size=min(n, B * H * N), replace=False))
         t0 = time.perf_counter()
-        oracle.attention(q, inp.k, inp.v, L, rows=rows)
+        oracle.attention(q, inp.k, inp.v, L, rows=np.arange(n) * (B * H * N // n))
         dt = time.perf_counter() - t0
-        if dt >= budget_s or n >= B * H * N:
-            return len(rows) * per_row / dt / 1e12, dt, len(rows), oracle.num_threads()
-        n = int(min(B * H * N, max(2 * n, n * budget_s / max(dt, 1e-3) * 1.1)))
+        if dt >= 0.25 * budget_s or n >= B * H * N:
+            return int(max(1, min(B * H * N, n * budget_s / max(dt, 1e-6))))
+        n = min(B * H * N, 4 * n)
+
+
+def oracle_run(w, inp, step, n_rows: int, seed: int = 0):
+    """Time the oracle on n_rows random query rows of `step`: (TFLOP/s, s, threads)."""
+    import oracle
+    q = inp.q[step]
+    B, H, N, D = q.shape
+    L = cache_len(w.sides, step)
+    rows = np.sort(np.random.default_rng(seed).choice(B * H * N, size=n_rows, replace=False))
+    t0 = time.perf_counter()
+    oracle.attention(q, inp.k, inp.v, L, rows=rows)
+    dt = time.perf_counter() - t0
+    return n_rows * 4.0 * L * D / dt / 1e12, dt, oracle.num_threads()
 
 
 def run_reference(args):
@@ -194,13 +208,15 @@ def run_reference(args):
     w = WORKLOADS[args.workload]
     step = w.steps[-1]
     inp = make_inputs(w, steps=(step,))
+    per_step = min(args.ref_seconds, 150.0 / (args.steps + args.warmup))
+    n_rows = oracle_calibrate(w, inp, step, per_step)
     vals = []
     for i in range(args.warmup + args.steps):
-        v, dt, nrows, thr = oracle_sample(w, inp, step, budget_s=args.ref_seconds)
+        tf, dt, thr = oracle_run(w, inp, step, n_rows, seed=i)
         if i >= args.warmup:
-            vals.append((v, dt, nrows))
-    value = statistics.median(v for v, _, _ in vals)
-    ms = statistics.median(dt for _, dt, _ in vals) * 1e3
+            vals.append((tf, dt))
+    value = statistics.median(v for v, _ in vals)
+    ms = statistics.median(dt for _, dt in vals) * 1e3
     q = inp.q[step]
     B, H, N, D = q.shape
     line = {
@@ -211,7 +227,8 @@ def run_reference(args):
         "config": {"workload": w.name, "batch": B, "heads": H, "head_dim": D, "queries": N,
                    "keys": cache_len(w.sides, step)},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
-                         "sample": f"{vals[-1][2]} query rows of the final step per timed step"},
+                         "sample": f"{n_rows} random query rows of the final step per step "
+                                   f"(of {B * H * N}); throughput scaled per FLOP"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -344,7 +361,14 @@ def run_gpu(args):
         step_fn()
     torch.cuda.synchronize()
     barrier(ws)
-    with ClockSampler(local) as clk:
+    with ClockSampler(local, enabled=not args.no_clocks) as clk:
+        if not args.no_clocks:
+            # keep the GPU busy (untimed) until the sampler is producing, then time
+            t0 = time.perf_counter()
+            while time.perf_counter() - t0 < 0.4:
+                step_fn()
+                torch.cuda.synchronize()
+            barrier(ws)
         ms = time_loop(step_fn, args.steps, stream)
     ms_max = reduce_max(ms, ws, dev)
     st = V.var_device_status()
@@ -394,9 +418,11 @@ def run_gpu(args):
     if not args.no_rows:
         line["rows"] = bench_rows(V, dev, stream, max(5, args.steps // 2))
     if rank == 0 and ws == 1 and not args.no_cpu:
-        tf, dt, nrows, thr = oracle_sample(w, inp, step, budget_s=args.cpu_seconds)
+        n_rows = oracle_calibrate(w, inp, step, args.cpu_seconds)
+        tf, dt, thr = oracle_run(w, inp, step, n_rows)
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
-                                "sample": f"{nrows} query rows of the final step ({dt:.1f} s)"}
+                                "sample": f"{n_rows} random query rows of the final step "
+                                          f"(of {B * H * N}), {dt:.1f} s; throughput per FLOP"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -408,12 +434,13 @@ def run_gpu(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("varattn", "reference"), default="varattn")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=HEADLINE)
     ap.add_argument("--no-rows", action="store_true", help="skip the per-kernel rows")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-clocks", action="store_true", help="no nvidia-smi sampling (profiler runs)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=3.0)
     args = ap.parse_args(argv)
