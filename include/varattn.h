@@ -107,6 +107,28 @@ VAR_API int var_pivot_select(const var_problem* p, int32_t step, const void* x, 
                      size_t workspace_bytes, void* stream);
 
 /*
+ * var_pivot_select without a caller-supplied workspace.  The pages have no
+ * counterpart to this entry point; it exists for callers that cannot allocate
+ * device memory where they select pivots -- an engine that owns all device
+ * memory and gives a plug-in no workspace, or a latency-critical stream on
+ * which cudaMalloc (which may synchronise the device) is not allowed after
+ * start-up.  It allocates nothing: its scratch is a file-scope device array
+ * of this library, sized for batch <= 4, N <= 16384 and channels <= 4096
+ * (about 1.9 MB, held on every GPU that loads the library until the process
+ * exits).  Larger problems return VAR_ERR_WORKSPACE and launch nothing.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array and it keeps the last call's
+ * contents (the accumulators that must start at zero are cleared on every
+ * call): calls whose work overlaps on the GPU -- on different streams, or
+ * from different host threads -- race and must be serialised by the caller.
+ * Arguments, results and other errors are those of var_pivot_select.
+ */
+VAR_API int var_pivot_select_noalloc(const var_problem* p, int32_t step, const void* x,
+                                     int32_t channels, int32_t keep_k, int32_t* idx,
+                                     float* scores, void* stream);
+
+/*
  * Pruned attention: dense attention for the kept query rows only, against the
  * full L-token cache ("FastVAR" abstract; "ARVAR" Key Design 2: only the
  * gathered positions undergo attention).

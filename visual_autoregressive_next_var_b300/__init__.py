@@ -62,6 +62,7 @@ _SIGS = {
     "var_pivot_workspace_bytes": (C.c_size_t, [_PROB, C.c_int32, C.c_int32]),
     "var_pivot_select": (C.c_int, [_PROB, C.c_int32, _P, C.c_int32, C.c_int32, _P, _P, _P,
                                    C.c_size_t, _P]),
+    "var_pivot_select_noalloc": (C.c_int, [_PROB, C.c_int32, _P, C.c_int32, C.c_int32, _P, _P, _P]),
     "var_attn_pruned": (C.c_int, [_PROB, C.c_int32, _P, _P, _P, _P, C.c_int32, _P, _P]),
     "var_restore_scatter": (C.c_int, [_PROB, C.c_int32, _P, _P, _P, C.c_int32, _P, _P]),
     "var_block_mask_build": (C.c_int, [_PROB, C.c_int32, C.c_int32, C.c_int32, C.c_int32, _P, _P,
@@ -149,6 +150,15 @@ def var_pivot_select(p: var_problem, step: int, x: torch.Tensor, keep_k: int, id
            _lib.var_pivot_select(C.byref(p), step, _ptr(x), channels, keep_k, _ptr(idx),
                                  _ptr(scores), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                  _stream(stream)))
+
+
+def var_pivot_select_noalloc(p: var_problem, step: int, x: torch.Tensor, keep_k: int, idx: torch.Tensor,
+                             scores: Optional[torch.Tensor] = None, stream=None) -> None:
+    """var_pivot_select with the library's own static scratch (no workspace argument)."""
+    channels = x.shape[-1]
+    _check("var_pivot_select_noalloc",
+           _lib.var_pivot_select_noalloc(C.byref(p), step, _ptr(x), channels, keep_k, _ptr(idx),
+                                         _ptr(scores), _stream(stream)))
 
 
 def var_attn_pruned(p: var_problem, step: int, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,

@@ -28,6 +28,7 @@
 // and FMA accumulation of q = C/32 terms per lane plus a 5-level shuffle tree
 // err <= (q + 9.1) u sum a_c^2 (u = 2^-24); eps uses 4u (q + 16) sum a_c^2.
 #include <cfloat>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -476,4 +477,71 @@ int launch_pivot_select(int B, int N, int C, const void* xv, int keep_k, int32_t
     return cuda_status(cudaGetLastError());
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free variant.  Some callers cannot allocate device memory at the
+// point where they select pivots: an engine that hands out all device memory
+// itself and gives a plug-in no workspace, or a latency-critical stream where
+// cudaMalloc (which may synchronise the device) is not allowed after start-up.
+// For them the workspace lives in this file-scope array instead, sized for
+// B <= 4, N <= 16384, C <= 4096 (about 1.9 MB).  Every GPU that loads the
+// library holds it until the process exits.
+
+constexpr int kNoAllocMaxB = 4;
+constexpr int kNoAllocMaxN = 16384;
+constexpr int kNoAllocMaxC = 4096;
+
+constexpr size_t noalloc_align(size_t x) { return (x + 255) & ~size_t(255); }
+constexpr size_t kNoAllocBytes =
+    noalloc_align(sizeof(long long) * kNoAllocMaxB * kNoAllocMaxC) * 2 +   // hi, lo
+    noalloc_align(sizeof(double) * kNoAllocMaxB * kNoAllocMaxC) +          // mean64
+    noalloc_align(sizeof(float) * kNoAllocMaxB * kNoAllocMaxC) +           // mean32
+    noalloc_align(sizeof(float) * kNoAllocMaxB * kNoAllocMaxN) * 2 +       // lo/hi keys
+    noalloc_align(sizeof(int) * kNoAllocMaxB * kNoAllocMaxN) +             // band indices
+    noalloc_align(sizeof(double) * kNoAllocMaxB * kNoAllocMaxN) +          // band scores
+    noalloc_align(sizeof(int) * kNoAllocMaxB * kNoAllocMaxN);              // flags
+
+static __device__ __align__(256) uint8_t g_pivot_scratch[kNoAllocBytes];
+
+// Device address of g_pivot_scratch on the current device.  Host code may not
+// use the symbol itself (it names a host-side shadow); the address is looked
+// up once per device, with that device current, and cached.
+static uint8_t* pivot_scratch_ptr()
+{
+    static std::mutex mu;
+    static uint8_t* cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!cache[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_pivot_scratch) != cudaSuccess || !p) return nullptr;
+        cache[dev] = static_cast<uint8_t*>(p);
+    }
+    return cache[dev];
+}
+
 }  // namespace varattn
+
+extern "C" int var_pivot_select_noalloc(const var_problem* p, int32_t step, const void* x,
+                                        int32_t channels, int32_t keep_k, int32_t* idx, float* scores,
+                                        void* stream)
+{
+    using namespace varattn;
+    if (!p || step < 0 || step >= p->n_scales || p->n_scales > VAR_MAX_SCALES) return VAR_ERR_INVALID_ARG;
+    if (p->batch <= 0 || p->side[step] <= 0 || p->side[step] > 4096) return VAR_ERR_INVALID_ARG;
+    if (!x || channels <= 0 || channels % 32 != 0) return VAR_ERR_INVALID_ARG;
+    const int B = p->batch;
+    const int N = p->side[step] * p->side[step];
+    if (keep_k < 0 || keep_k > N) return VAR_ERR_INVALID_ARG;
+    if (keep_k > 0 && !idx) return VAR_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(x) & 15u) != 0) return VAR_ERR_UNSUPPORTED;
+    if (B > kNoAllocMaxB || N > kNoAllocMaxN || channels > kNoAllocMaxC) return VAR_ERR_WORKSPACE;
+    const size_t need = pivot_workspace_bytes(B, N, channels);
+    if (need > kNoAllocBytes) return VAR_ERR_WORKSPACE;
+    uint8_t* ws = pivot_scratch_ptr();
+    if (!ws) return VAR_ERR_CUDA;
+    // launch_pivot_select clears the accumulators it needs zeroed (cudaMemsetAsync,
+    // no allocation); everything else in the scratch is written before it is read.
+    return launch_pivot_select(B, N, channels, x, keep_k, idx, scores, ws, kNoAllocBytes,
+                               static_cast<cudaStream_t>(stream));
+}
