@@ -6,7 +6,7 @@ torch's current CUDA stream unless one is given, and a non-zero status raises
 ``VarError``.  PyTorch is used only to own device memory and streams.
 
 Importing this module loads the shared library and fails loudly if it is
-missing; run ``python -m visual_autoregressive_next_var_b300.build`` (or
+missing; run ``python visual_autoregressive_next_var_b300/build.py`` (or
 ``__graft_entry__.build()``) first.
 """
 from __future__ import annotations
@@ -52,7 +52,7 @@ class var_block_mask(C.Structure):
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build the CUDA library first "
-                      "(python -m visual_autoregressive_next_var_b300.build)")
+                      "(python visual_autoregressive_next_var_b300/build.py)")
 _lib = C.CDLL(LIB_PATH)
 
 _P = C.c_void_p
