@@ -310,7 +310,6 @@ def bench_rows(V, dev, stream, steps: int):
         t_bs = time_loop(bs, steps, stream)
         N = q.shape[2]
         L = cache_len(w.sides, step)
-        kept = (int(row_ptr[-1]) * 64 + (len(row_ptr) - 1) * sink_len) * 64  # approx upper bound
         # algorithmic FLOPs: 4*D per kept (query, key) pair, from the CSR
         kept_pairs = 0
         sides = w.sides
@@ -326,7 +325,6 @@ def bench_rows(V, dev, stream, steps: int):
                                        "frac_tensor": fl / t_bs / 1e9 / peaks["bf16_tflops"],
                                        "dense_equiv_TFLOP/s": 4.0 * B * H * N * L * D / t_bs / 1e9,
                                        "density": kept_pairs / (N * L)}
-        del kept
     except V.VarError as e:
         rows["attn_blocksparse_2k"] = {"unavailable": str(e)}
     return rows
@@ -404,11 +402,11 @@ def run_gpu(args):
                    "keys": L, "kv_tokens_total": inp.k.shape[2],
                    "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB of Q/K/V)",
                    "per_gpu": "each rank runs the whole workload"},
-        "roofline": {"kernel": "attn_fwd_kernel<128,false>", "bound": "tensor", "achieved": achieved,
+        "roofline": {"kernel": "attn_kernel<128, dense>", "bound": "tensor", "achieved": achieved,
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / peaks["bf16_tflops"],
                      "peak_source": f"{peaks['source']} dense bf16 burst (cuBLAS)",
-                     "traffic": ncu_traffic("attn_fwd_kernel<128,false>:" + w.name, 1.0),
+                     "traffic": ncu_traffic("attn_kernel<128, dense>:" + w.name, 1.0),
                      "algorithmic_flops_per_launch": flops},
         "e2e": {"value": ws * flops / ms_e2e / 1e9, "unit": "TFLOP/s", "ms_per_step": ms_e2e,
                 "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": o.numel() * 2},
