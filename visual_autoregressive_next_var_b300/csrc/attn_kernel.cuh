@@ -583,9 +583,19 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
                         if (c >= valid) s[c >> 5][c & 31] = __float_as_uint(-INFINITY);
                 }
             }
-            float mx = -INFINITY;
+            // row maximum: eight independent chains of 3-input max
+            float mc[8];
 #pragma unroll
-            for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c >> 5][c & 31]));
+            for (int q = 0; q < 8; ++q) {
+                const int base = q * 16;      // chain q covers columns [16q, 16q + 16)
+                float m = __uint_as_float(s[base >> 5][base & 31]);
+#pragma unroll
+                for (int c = 1; c < 15; c += 2)
+                    m = fmax3(m, __uint_as_float(s[(base + c) >> 5][(base + c) & 31]),
+                              __uint_as_float(s[(base + c + 1) >> 5][(base + c + 1) & 31]));
+                mc[q] = fmaxf(m, __uint_as_float(s[(base + 15) >> 5][(base + 15) & 31]));
+            }
+            const float mx = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
             const float m_tile = mx * sl2;
             const bool need = m_tile > m_run + 8.0f;
             const float m_new = need ? m_tile : m_run;
@@ -594,21 +604,28 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
             m_run = m_new;
             // P = exp2(S * scale*log2e - m), packed to bf16 pairs, 16 columns at a time
             const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-            float sum0 = 0.f, sum1 = 0.f;
+            const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(neg_m, neg_m);
+            uint64_t sum2 = f2_pack(0.f, 0.f);
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(s[cc][2 * c]), sl2, neg_m));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(s[cc][2 * c + 1]), sl2, neg_m));
-                    sum0 += p0;
-                    sum1 += p1;
+                    const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(s[cc][2 * c]), __uint_as_float(s[cc][2 * c + 1])),
+                                               sc2, nm2);
+                    float x0, x1;
+                    f2_unpack(x2, x0, x1);
+                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                    sum2 = f2_add(sum2, f2_pack(p0, p1));
                     pk[c] = pack_bf16x2(p0, p1);
                 }
                 tmem_st16(tS + cc * 16, pk);
             }
-            l_run += sum0 + sum1;
+            {
+                float a0, a1;
+                f2_unpack(sum2, a0, a1);
+                l_run += a0 + a1;
+            }
             // O_t *= alpha where the running maximum moved (the previous PV has
             // completed: its commit preceded this tile's S commit)
             if (__any_sync(0xffffffffu, need && j > 0)) {
