@@ -91,9 +91,12 @@ VAR_API size_t var_pivot_workspace_bytes(const var_problem* p, int32_t step, int
  *   score[b,i] = ||x[b,i,:] - m_b||_2^2
  * keeps the keep_k largest scores (equal scores: the lower flat index first)
  * and writes their indices in ascending order.  The ranking is that of the
- * fp64 evaluation (channel sums as a pairwise-halving tree): fp32 scores
- * decide every token outside a certified error band; band tokens are
- * re-scored in fp64 on the device.
+ * fp64 evaluation (exact channel sums, fp64 mean, squared differences summed
+ * as a pairwise-halving tree over channels): fp32 scores with a certified
+ * error bound decide every token outside a narrow band around the K-th score;
+ * band tokens are decided by count or re-scored in fp64 on the device.
+ * Two kernels on `stream`, the second launched as a programmatic dependent of
+ * the first.
  * x: [B][N][channels] bf16, channels a positive multiple of 32, |x| < 2^20.
  * idx: [B][keep_k] int32 (device).  scores: optional [B][N] fp32 (device) or NULL.
  * workspace: device memory of var_pivot_workspace_bytes() bytes, 256-byte
@@ -114,14 +117,15 @@ VAR_API int var_pivot_select(const var_problem* p, int32_t step, const void* x, 
  * which cudaMalloc (which may synchronise the device) is not allowed after
  * start-up.  It allocates nothing: its scratch is a file-scope device array
  * of this library, sized for batch <= 4, N <= 16384 and channels <= 4096
- * (about 1.9 MB, held on every GPU that loads the library until the process
+ * (about 1.5 MB, held on every GPU that loads the library until the process
  * exits).  Larger problems return VAR_ERR_WORKSPACE and launch nothing.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
  * capture.  All calls share the one array and it keeps the last call's
- * contents (the accumulators that must start at zero are cleared on every
- * call): calls whose work overlaps on the GPU -- on different streams, or
- * from different host threads -- race and must be serialised by the caller.
+ * contents (nothing in it needs clearing: each call writes every word it
+ * reads, and resets its own completion counters): calls whose work overlaps
+ * on the GPU -- on different streams, or from different host threads -- race
+ * and must be serialised by the caller.
  * Arguments, results and other errors are those of var_pivot_select.
  */
 VAR_API int var_pivot_select_noalloc(const var_problem* p, int32_t step, const void* x,

@@ -75,6 +75,40 @@ def test_pivot_ties_and_degenerate_grids():
     check_device_status()
 
 
+def test_pivot_outliers_and_tiny_values():
+    """Elements at or beyond the fast summation window (|x| >= 512) and far below
+    it (|x| < 2^-29, zeros) must still give the oracle's exact ranking."""
+    p = V.problem(2, 1, 64, (1, 24))
+    x = randn_bf16((2, 576, 160), 62).float()
+    x[0, 5, 3] = 1000.0
+    x[0, 300, 100] = -700.0
+    x[1, 17, 0] = 512.0
+    x[1, 200, :] = 3e-10
+    x[1, 201, 7] = 0.0
+    x[0, 400:410, 40] = 1e-12
+    x = x.to(torch.bfloat16)
+    for K in (1, 57, 300):
+        got, sc = gpu_pivot(p, 1, x, K, want_scores=True)
+        ref, ref_sc = oracle.pivot_select(x, K)
+        assert np.array_equal(got, ref), K
+        assert np.max(np.abs(sc - ref_sc) / np.maximum(ref_sc, 1.0)) < 1e-4
+    check_device_status()
+
+
+def test_pivot_single_token_and_large_grid():
+    p = V.problem(1, 1, 64, (1, 2))
+    x1 = randn_bf16((1, 1, 32), 63)
+    got, _ = gpu_pivot(p, 0, x1, 1)
+    assert np.array_equal(got, [[0]])
+    sides = (1, 2, 4, 8, 16, 32, 64, 128)
+    q = V.problem(1, 1, 64, sides)
+    x = randn_bf16((1, 16384, 256), 64)
+    got, _ = gpu_pivot(q, 7, x, 3277)
+    ref, _ = oracle.pivot_select(x, 3277)
+    assert np.array_equal(got, ref)
+    check_device_status()
+
+
 # ---------------------------------------------------------------- pruned attention
 
 @pytest.mark.parametrize("K", [1, 130, 819, 4096])
