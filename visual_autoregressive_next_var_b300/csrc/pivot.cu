@@ -12,23 +12,25 @@
 //
 //   1. colsum (HBM pass over X).  Exact channel sums.  A cluster of 8 CTAs
 //      owns a 128-channel chunk of one batch element, each CTA a slab of
-//      rows.  Per element: x = hi + lo split exactly by two fp32 "magic"
-//      additions (hi a multiple of 2^-13, |x| < 512; lo a multiple of 2^-36),
-//      the float bit patterns summed as wrapping 32-bit integers, which is an
-//      exact fixed-point sum.  A thread that meets |x| >= 512 redoes its rows
-//      with 64-bit fixed point.  The cluster merges its CTAs' partial sums
-//      through distributed shared memory; the exact sum is rounded once to
-//      fp64, divided by N (the fp64 mean), and rounded to fp32 for the scores.
-//      Launches the score kernel early (programmatic dependent launch).
-//   2. score + select (L2 pass over X).  One warp per token: fp32 score with
-//      a rigorous bound eps_i >= |fp32 score - fp64 score| (below), stored as
+//      rows streamed through a cp.async ring in shared memory.  Per element:
+//      x = hi + lo split exactly by two fp32 "magic" additions (hi a multiple
+//      of 2^-13, |x| < 512; lo a multiple of 2^-36), the float bit patterns
+//      summed as wrapping 32-bit integers, which is an exact fixed-point sum.
+//      A thread that meets |x| >= 512 redoes its rows in 64-bit fixed point.
+//      The cluster merges its CTAs' partial sums through distributed shared
+//      memory; the exact sum is rounded once to fp64, divided by N (the fp64
+//      mean), and rounded to fp32 for the scores.
+//   2. score (L2 pass over X).  One warp per token: fp32 score with a
+//      rigorous bound eps_i >= |fp32 score - fp64 score| (below), stored as
 //      lo_i = score - eps (rounded down), hi_i = score + eps (rounded up).
-//      The last CTA of a batch element to finish selects: T_lo = K-th largest
-//      lo, T_hi = (K+1)-th largest hi (radix select); lo_i > T_hi => certainly
-//      kept, hi_i < T_lo => certainly dropped; the band in between is either
-//      decided by count (all kept or all dropped) or re-scored in fp64 in the
-//      exact evaluation order, the remaining slots going to the best band
-//      tokens by (score desc, index asc).  Output compaction keeps order.
+//   3. select, one 1024-thread CTA per batch element, keys in registers:
+//      T_lo = K-th largest lo, T_hi = (K+1)-th largest hi (histogram
+//      narrowing, then brute force on a small range); lo_i > T_hi =>
+//      certainly kept, hi_i < T_lo => certainly dropped; the band in between
+//      is decided by count (all kept or all dropped) or re-scored in fp64 in
+//      the exact evaluation order, the remaining slots going to the best band
+//      tokens by (score desc, index asc).  Compaction keeps ascending order.
+//   Kernels 2 and 3 are programmatic dependent launches of their predecessor.
 //
 // Error bound of kernel 2.  m' is the fp32 mean, mu the exact mean,
 // E >= ||m' - mu||_2 = 2^-24 ||m'|| (1 + 2^-23) + 2^-120.  A lane sums its
@@ -52,23 +54,30 @@ namespace {
 constexpr int kSlabs = 8;                 // CTAs per cluster: row slabs of one chunk
 constexpr int kChunk = 128;               // channels per chunk (256 bytes of a row)
 constexpr int kSegs = kChunk / 8;         // 16-byte segments of a chunk row
-constexpr int kSumThreads = 256;
-constexpr int kRowGroups = kSumThreads / kSegs;   // rows in flight per CTA pass
-constexpr int kSumUnroll = 8;
+constexpr int kSumThreads = 512;
+constexpr int kRowGroups = kSumThreads / kSegs;   // rows per CTA pass (a thread takes 2 per stage)
+constexpr int kStageRows = 64;            // rows per cp.async stage (16 KB)
+constexpr int kStages = 4;                // stages in flight
+constexpr int kRingBytes = kStages * kStageRows * kChunk * 2;
 
 constexpr int kScoreThreads = 256;
 constexpr int kScoreWarps = kScoreThreads / 32;
 constexpr int kTokPerWarp = 2;
 constexpr int kScoreTok = kScoreWarps * kTokPerWarp;   // tokens per score CTA
 
-constexpr int kScoreSmemMax = 220 * 1024;    // dynamic shared memory cap of the score kernel
+constexpr int kSelThreads = 1024;
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kMaxKeysPerThread = 16;     // N <= kSelThreads * kMaxKeysPerThread
+constexpr int kMaxN = kSelThreads * kMaxKeysPerThread;
+constexpr int kSelBins = 2048;            // histogram bins per narrowing level (power of two)
+constexpr int kSelCand = 256;             // ranges this small are ranked by brute force
 
 constexpr float kMagA = 1536.0f;          // 1.5 * 2^10: ulp 2^-13 on [1024, 2048)
 constexpr float kMagB = 0x1.8p-13f;       // 1.5 * 2^-13: ulp 2^-36 on [2^-13, 2^-12)
 constexpr float kFastMax = 512.0f;        // |x| below this takes the two-window path
 
 struct PivotWs {
-    size_t mean64, mean32, lok, hik, band_idx, band_score, counters, total;
+    size_t mean64, mean32, lok, hik, band_idx, band_score, total;
 };
 
 __host__ __device__ constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -83,21 +92,11 @@ __host__ __device__ constexpr PivotWs pivot_ws_layout(int B, int N, int C)
     w.hik = o;        o = align256(o + sizeof(float) * B * N);
     w.band_idx = o;   o = align256(o + sizeof(int) * B * N);
     w.band_score = o; o = align256(o + sizeof(double) * B * N);
-    w.counters = o;   o = align256(o + sizeof(int) * B);
     w.total = o;
     return w;
 }
 
 // ------------------------------------------------------------------ PTX helpers
-
-__device__ __forceinline__ uint4 ld_stream16(const void* p)
-{
-    uint4 v;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-        : "l"(p));
-    return v;
-}
 
 __device__ __forceinline__ void cluster_sync_all()
 {
@@ -128,6 +127,16 @@ __device__ __forceinline__ void pdl_wait()
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int n>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory"); }
 
 __device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b)
 {
@@ -177,111 +186,169 @@ __device__ double i128_to_f64_rn(__int128 t)
     return neg ? -r : r;
 }
 
+// Adds rows a and b of 8 channels (one 16-byte word each) to the two-window
+// fixed-point sums: acc_a in ulps of 2^-13 (plus bits(kMagA) per row), acc_b
+// in ulps of 2^-36 (plus bits(kMagB) per row); mx tracks max |x|.
+__device__ __forceinline__ void accum_rows2(const uint4& va, const uint4& vb, uint32_t (&acc_a)[8],
+                                            uint32_t (&acc_b)[8], float& mx)
+{
+    const uint64_t mag_a = f2_pack(kMagA, kMagA), mag_b = f2_pack(kMagB, kMagB);
+    const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
+    const uint32_t wb[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        float sa[2], ta[2], sb[2], tb[2];
+        {
+            const float x0 = __uint_as_float(wa[e] << 16), x1 = __uint_as_float(wa[e] & 0xFFFF0000u);
+            const uint64_t x2 = f2_pack(x0, x1);
+            const uint64_t s2 = f2_add(x2, mag_a);                 // RN(x + 1.5*2^10)
+            const uint64_t l2 = f2_sub(x2, f2_sub(s2, mag_a));     // x - hi, exact
+            const uint64_t t2 = f2_add(l2, mag_b);                 // RN(lo + 1.5*2^-13), exact
+            f2_unpack(s2, sa[0], sa[1]);
+            f2_unpack(t2, ta[0], ta[1]);
+            mx = fmax3(mx, fabsf(x0), fabsf(x1));
+        }
+        {
+            const float x0 = __uint_as_float(wb[e] << 16), x1 = __uint_as_float(wb[e] & 0xFFFF0000u);
+            const uint64_t x2 = f2_pack(x0, x1);
+            const uint64_t s2 = f2_add(x2, mag_a);
+            const uint64_t l2 = f2_sub(x2, f2_sub(s2, mag_a));
+            const uint64_t t2 = f2_add(l2, mag_b);
+            f2_unpack(s2, sb[0], sb[1]);
+            f2_unpack(t2, tb[0], tb[1]);
+            mx = fmax3(mx, fabsf(x0), fabsf(x1));
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            acc_a[2 * e + h] += __float_as_uint(sa[h]) + __float_as_uint(sb[h]);
+            acc_b[2 * e + h] += __float_as_uint(ta[h]) + __float_as_uint(tb[h]);
+        }
+    }
+}
+
 __global__ void __cluster_dims__(kSlabs, 1, 1) __launch_bounds__(kSumThreads)
     pivot_colsum_kernel(const __nv_bfloat16* __restrict__ x, int N, int C, double* __restrict__ mean64,
-                        float* __restrict__ mean32, int* __restrict__ counters, int32_t* status)
+                        float* __restrict__ mean32, int32_t* status)
 {
-    __shared__ long long red_p[kRowGroups][kChunk];
-    __shared__ long long red_q[kRowGroups][kChunk];
-    __shared__ __align__(16) long long part[kChunk][2];   // this CTA's (p, q) per channel
+    extern __shared__ __align__(128) uint8_t ring[];                // [kStages][kStageRows][kChunk] bf16
+    __shared__ __align__(16) long long part[kChunk][2];              // this CTA's (p, q) per channel
 
     pdl_launch_dependents();
-    const int rank = static_cast<int>(cluster_rank());    // == blockIdx.x (cluster spans x)
+    const int rank = static_cast<int>(cluster_rank());    // == blockIdx.x (the cluster spans x)
     const int chunk = blockIdx.y, b = blockIdx.z;
-    const int rg = threadIdx.x / kSegs, seg = threadIdx.x % kSegs;
+    const int tid = threadIdx.x;
+    const int rg = tid / kSegs, seg = tid % kSegs;
     const int c = chunk * kChunk + seg * 8;
+    const bool cvalid = c < C;
     const int slab = (N + kSlabs - 1) / kSlabs;
     const int r0 = min(N, rank * slab), r1 = min(N, r0 + slab);
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) counters[b] = 0;
+    const int nstage = (r1 - r0 + kStageRows - 1) / kStageRows;
+    const __nv_bfloat16* base = x + static_cast<size_t>(b) * N * C + c;
+    const uint32_t ring_s = smem_u32(ring);
+
+    // stage st: rows r0 + st*64 + [0, 64); this thread copies rows rg and rg + kRowGroups
+    auto issue = [&](int st) {
+        if (st < nstage && cvalid) {
+            const int rbase = r0 + st * kStageRows;
+            const uint32_t slot = ring_s + static_cast<uint32_t>((st % kStages) * kStageRows * kChunk * 2);
+#pragma unroll
+            for (int j = 0; j < kStageRows / kRowGroups; ++j) {
+                const int rr = rg + kRowGroups * j;
+                if (rbase + rr < r1)
+                    cp_async16(slot + static_cast<uint32_t>(rr * kChunk * 2 + seg * 16),
+                               base + static_cast<size_t>(rbase + rr) * C);
+            }
+        }
+        cp_async_commit();
+    };
+
+    uint32_t acc_a[8], acc_b[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc_a[e] = acc_b[e] = 0u;
+    float mx = 0.f;
+    static_assert(kStageRows == 2 * kRowGroups, "a thread takes rows rg and rg + kRowGroups of a stage");
+#pragma unroll
+    for (int st = 0; st < kStages - 1; ++st) issue(st);
+    for (int st = 0; st < nstage; ++st) {
+        issue(st + kStages - 1);
+        cp_async_wait<kStages - 1>();
+        __syncthreads();
+        if (cvalid) {
+            const uint8_t* slot = ring + (st % kStages) * kStageRows * kChunk * 2 + seg * 16;
+            const int rows = min(kStageRows, r1 - r0 - st * kStageRows);
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            uint4 va, vb;
+            if (rows == kStageRows) {
+                va = *reinterpret_cast<const uint4*>(slot + rg * kChunk * 2);
+                vb = *reinterpret_cast<const uint4*>(slot + (rg + kRowGroups) * kChunk * 2);
+            } else {                                   // rows past the slab add x = 0
+                va = rg < rows ? *reinterpret_cast<const uint4*>(slot + rg * kChunk * 2) : z;
+                vb = rg + kRowGroups < rows ? *reinterpret_cast<const uint4*>(slot + (rg + kRowGroups) * kChunk * 2) : z;
+            }
+            accum_rows2(va, vb, acc_a, acc_b, mx);
+        }
+        __syncthreads();
+    }
+    cp_async_wait<0>();
 
     // exact sum of this thread's elements = p * 2^-24 + q * 2^-60
     long long p[8], q[8];
     bool bad = false;
-    if (c < C) {
-        const __nv_bfloat16* base = x + static_cast<size_t>(b) * N * C + c;
-        uint32_t acc_a[8], acc_b[8];
+    if (mx < kFastMax) {
+        // every row slot added bits(M) + (its value in ulps of the window)
+        const uint32_t nr = static_cast<uint32_t>(nstage * 2);          // row slots per thread
+        const uint32_t bias_a = nr * __float_as_uint(kMagA), bias_b = nr * __float_as_uint(kMagB);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc_a[e] = acc_b[e] = 0u;
-        float mx = 0.f;
-        const uint64_t mag_a = f2_pack(kMagA, kMagA), mag_b = f2_pack(kMagB, kMagB);
-        auto accum = [&](const uint4& v) {
+        for (int e = 0; e < 8; ++e) {
+            p[e] = static_cast<long long>(static_cast<int32_t>(acc_a[e] - bias_a)) * (1ll << 11);
+            q[e] = static_cast<long long>(static_cast<int32_t>(acc_b[e] - bias_b)) * (1ll << 24);
+        }
+    } else {
+        // an element at or beyond the fast window: redo these rows in 64-bit fixed point
+#pragma unroll
+        for (int e = 0; e < 8; ++e) p[e] = q[e] = 0;
+        for (int rr = r0 + rg; rr < r1; rr += kRowGroups) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(base + static_cast<size_t>(rr) * C));
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float x0 = __uint_as_float(w[e] << 16), x1 = __uint_as_float(w[e] & 0xFFFF0000u);
-                const uint64_t x2 = f2_pack(x0, x1);
-                const uint64_t s2 = f2_add(x2, mag_a);                 // RN(x + 1.5*2^10)
-                const uint64_t l2 = f2_sub(x2, f2_sub(s2, mag_a));     // x - hi, exact
-                const uint64_t t2 = f2_add(l2, mag_b);                 // RN(lo + 1.5*2^-13)
-                float s0, s1, t0, t1;
-                f2_unpack(s2, s0, s1);
-                f2_unpack(t2, t0, t1);
-                acc_a[2 * e] += __float_as_uint(s0);
-                acc_a[2 * e + 1] += __float_as_uint(s1);
-                acc_b[2 * e] += __float_as_uint(t0);
-                acc_b[2 * e + 1] += __float_as_uint(t1);
-                mx = fmax3(mx, fabsf(x0), fabsf(x1));
-            }
-        };
-        int r = r0 + rg;
-        for (; r + kRowGroups * (kSumUnroll - 1) < r1; r += kRowGroups * kSumUnroll) {
-            uint4 v[kSumUnroll];
-#pragma unroll
-            for (int u = 0; u < kSumUnroll; ++u) v[u] = ld_stream16(base + static_cast<size_t>(r + kRowGroups * u) * C);
-#pragma unroll
-            for (int u = 0; u < kSumUnroll; ++u) accum(v[u]);
-        }
-        for (; r < r1; r += kRowGroups) accum(ld_stream16(base + static_cast<size_t>(r) * C));
-        const int nr = r0 + rg < r1 ? (r1 - r0 - rg + kRowGroups - 1) / kRowGroups : 0;
-        if (mx < kFastMax) {
-            // every element added bits(M) + (its value in ulps of the window)
-            const uint32_t bias_a = static_cast<uint32_t>(nr) * __float_as_uint(kMagA);
-            const uint32_t bias_b = static_cast<uint32_t>(nr) * __float_as_uint(kMagB);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                p[e] = static_cast<long long>(static_cast<int32_t>(acc_a[e] - bias_a)) * (1ll << 11);
-                q[e] = static_cast<long long>(static_cast<int32_t>(acc_b[e] - bias_b)) * (1ll << 24);
-            }
-        } else {
-            // an element at or beyond the fast window: redo these rows in 64-bit fixed point
-#pragma unroll
-            for (int e = 0; e < 8; ++e) p[e] = q[e] = 0;
-            for (int rr = r0 + rg; rr < r1; rr += kRowGroups) {
-                const uint4 v = ld_stream16(base + static_cast<size_t>(rr) * C);
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    accum_fixed(w[e] & 0xFFFFu, p[2 * e], q[2 * e], bad);
-                    accum_fixed(w[e] >> 16, p[2 * e + 1], q[2 * e + 1], bad);
-                }
+                accum_fixed(w[e] & 0xFFFFu, p[2 * e], q[2 * e], bad);
+                accum_fixed(w[e] >> 16, p[2 * e + 1], q[2 * e + 1], bad);
             }
         }
-    } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) p[e] = q[e] = 0;
     }
     if (bad) atomicCAS(status, 0, VAR_ERR_NUMERIC);
+    // the two row groups of a warp share channels (lanes l and l ^ 16)
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-        red_p[rg][seg * 8 + e] = p[e];
-        red_q[rg][seg * 8 + e] = q[e];
+        p[e] += __shfl_xor_sync(0xffffffffu, p[e], 16);
+        q[e] += __shfl_xor_sync(0xffffffffu, q[e], 16);
+    }
+    long long* red = reinterpret_cast<long long*>(ring);    // [warps][kChunk][2], the ring is idle now
+    const int warp = tid >> 5, lane = tid & 31;
+    if (lane < 16) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            red[(warp * kChunk + seg * 8 + e) * 2] = p[e];
+            red[(warp * kChunk + seg * 8 + e) * 2 + 1] = q[e];
+        }
     }
     __syncthreads();
-    if (threadIdx.x < kChunk) {
+    if (tid < kChunk) {
         long long sp = 0, sq = 0;
 #pragma unroll
-        for (int g = 0; g < kRowGroups; ++g) {
-            sp += red_p[g][threadIdx.x];
-            sq += red_q[g][threadIdx.x];
+        for (int w = 0; w < kSumThreads / 32; ++w) {
+            sp += red[(w * kChunk + tid) * 2];
+            sq += red[(w * kChunk + tid) * 2 + 1];
         }
-        part[threadIdx.x][0] = sp;
-        part[threadIdx.x][1] = sq;
+        part[tid][0] = sp;
+        part[tid][1] = sq;
     }
     cluster_sync_all();
     // CTA `rank` finishes channels [rank*16, rank*16 + 16) of the chunk
     constexpr int kPer = kChunk / kSlabs;
-    if (threadIdx.x < kPer) {
-        const int cl = rank * kPer + threadIdx.x;
+    if (tid < kPer) {
+        const int cl = rank * kPer + tid;
         const int cc = chunk * kChunk + cl;
         long long sp = 0, sq = 0;
         const uint32_t la = smem_u32(&part[cl][0]);
@@ -303,134 +370,18 @@ __global__ void __cluster_dims__(kSlabs, 1, 1) __launch_bounds__(kSumThreads)
     cluster_sync_all();    // peers may still be reading this CTA's partial sums
 }
 
-// ------------------------------------------------------------------ 2. score + select
+// ------------------------------------------------------------------ 2. score
 
-// Order-preserving map float -> uint32 (larger float -> larger key).
-__device__ __forceinline__ uint32_t f32_key(float f)
+__global__ void __launch_bounds__(kScoreThreads, 4)
+    pivot_score_kernel(const __nv_bfloat16* __restrict__ x, int N, int C, const float* __restrict__ mean32,
+                       float* __restrict__ lo_g, float* __restrict__ hi_g, float* __restrict__ scores,
+                       int32_t* status)
 {
-    const uint32_t u = __float_as_uint(f);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// fp64 score of one token in the exact evaluation order: lane l sums channels
-// [l*q, (l+1)*q) as a halving tree, the 32 lane sums are combined pairwise by
-// the xor butterfly (the top five levels of the same tree; C = 32 q).
-__device__ double tree64(const __nv_bfloat16* x, const double* m, int n)
-{
-    if (n == 1) {
-        const double d = __dsub_rn(static_cast<double>(__bfloat162float(x[0])), m[0]);
-        return __dmul_rn(d, d);
-    }
-    const int h = n / 2;
-    const double a = tree64(x, m, h);
-    const double bb = tree64(x + h, m + h, n - h);
-    return __dadd_rn(a, bb);
-}
-
-// The rank-`ra`-largest of ka[0..n) and the rank-`rb`-largest of kb[0..n)
-// (1-based), by 8-bit radix select with warp-aggregated shared histograms.
-// All threads of the CTA call it.
-__device__ void dual_radix_select(const uint32_t* ka, int ra, const uint32_t* kb, int rb, int n,
-                                  int (*hist)[256], int* sel, uint32_t& out_a, uint32_t& out_b)
-{
-    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
-    uint32_t pre_a = 0, pre_b = 0, msk = 0;
-    int want_a = ra, want_b = rb;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int j = tid; j < 512; j += nt) hist[j >> 8][j & 255] = 0;
-        __syncthreads();
-        for (int base = warp * 32; base < n; base += nt) {
-            const int i = base + lane;
-            uint32_t da = 0xFFFFFFFFu, db = 0xFFFFFFFFu;
-            if (i < n) {
-                const uint32_t a = ka[i], bb = kb[i];
-                if ((a & msk) == pre_a) da = (a >> shift) & 255u;
-                if ((bb & msk) == pre_b) db = (bb >> shift) & 255u;
-            }
-            const uint32_t pa = __match_any_sync(0xffffffffu, da);
-            if (da != 0xFFFFFFFFu && lane == __ffs(pa) - 1) atomicAdd(&hist[0][da], __popc(pa));
-            const uint32_t pb = __match_any_sync(0xffffffffu, db);
-            if (db != 0xFFFFFFFFu && lane == __ffs(pb) - 1) atomicAdd(&hist[1][db], __popc(pb));
-        }
-        __syncthreads();
-        if (warp < 2) {
-            // lane l owns digits 255-8l .. 248-8l (descending)
-            const int* hh = hist[warp];
-            const int want = warp ? want_b : want_a;
-            int cnt[8];
-            int tot = 0;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                cnt[k] = hh[255 - 8 * lane - k];
-                tot += cnt[k];
-            }
-            int incl = tot;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += v;
-            }
-            const int excl = incl - tot;
-            if (excl < want && want <= incl) {
-                int run = excl;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    if (run < want && want <= run + cnt[k]) {
-                        sel[2 * warp] = 255 - 8 * lane - k;
-                        sel[2 * warp + 1] = want - run;
-                    }
-                    run += cnt[k];
-                }
-            }
-        }
-        __syncthreads();
-        pre_a |= static_cast<uint32_t>(sel[0]) << shift;
-        want_a = sel[1];
-        pre_b |= static_cast<uint32_t>(sel[2]) << shift;
-        want_b = sel[3];
-        msk |= 0xFFu << shift;
-    }
-    out_a = pre_a;
-    out_b = pre_b;
-}
-
-// Exclusive prefix over the CTA's warps of per-warp totals v (lane-uniform);
-// returns this warp's offset and writes the total.  All threads call it.
-__device__ __forceinline__ int warp_offsets(int v, int* scratch, int* total)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    if (lane == 0) scratch[warp] = v;
-    __syncthreads();
-    int off = 0, tot = 0;
-    for (int w = 0; w < nw; ++w) {
-        const int s = scratch[w];
-        off += w < warp ? s : 0;
-        tot += s;
-    }
-    __syncthreads();
-    *total = tot;
-    return off;
-}
-
-__global__ void __launch_bounds__(kScoreThreads)
-    pivot_score_kernel(const __nv_bfloat16* __restrict__ x, int N, int C, int K, const float* __restrict__ mean32,
-                       const double* __restrict__ mean64, float* __restrict__ lo_g, float* __restrict__ hi_g,
-                       float* __restrict__ scores, int* __restrict__ counters, int* __restrict__ band_idx_g,
-                       double* __restrict__ band_score_g, int32_t* __restrict__ idx_out, int32_t* status)
-{
-    extern __shared__ __align__(16) uint8_t psm[];
-    float* m_s = reinterpret_cast<float*>(psm);                                   // [C]
-    uint32_t* klo = reinterpret_cast<uint32_t*>(psm + ((static_cast<size_t>(C) * 4 + 15) & ~size_t(15)));  // [N]
-    uint32_t* khi = klo + N;                                                      // [N]
-    uint8_t* flg = reinterpret_cast<uint8_t*>(khi + N);                           // [N]
-    __shared__ int hist[2][256];
-    __shared__ int sel[4];
-    __shared__ int wsc[kScoreWarps];
+    extern __shared__ __align__(16) float m_s[];   // [C]
     __shared__ float red[kScoreWarps];
-    __shared__ int is_last;
-
     const int b = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_launch_dependents();
     pdl_wait();   // the channel means of the colsum kernel
 
     float ss = 0.f;
@@ -455,42 +406,69 @@ __global__ void __launch_bounds__(kScoreThreads)
     const float mn2 = __fadd_ru(__fmul_ru(mn, mn), 1.f);
     const uint64_t neg1 = f2_pack(-1.f, -1.f);
 
+    // the warp's tokens are scored together: one read of the means serves both
+    const int i0 = blockIdx.x * kScoreTok + warp * kTokPerWarp;
+    const uint4* rows[kTokPerWarp];
+    bool tv[kTokPerWarp];
+#pragma unroll
     for (int t = 0; t < kTokPerWarp; ++t) {
-        const int i = blockIdx.x * kScoreTok + warp * kTokPerWarp + t;
-        if (i >= N) break;
-        const uint4* row = reinterpret_cast<const uint4*>(x + (static_cast<size_t>(b) * N + i) * C);
-        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-        for (int k0 = 0; k0 < h1; k0 += 8) {
-            uint4 v[8];
+        tv[t] = i0 + t < N;
+        rows[t] = reinterpret_cast<const uint4*>(x + (static_cast<size_t>(b) * N + min(i0 + t, N - 1)) * C);
+    }
+    uint64_t acc[kTokPerWarp][4];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int ch = lane + 32 * (k0 + k);
-                v[k] = ch < nchunk ? __ldg(row + ch) : make_uint4(0u, 0u, 0u, 0u);
-            }
+    for (int t = 0; t < kTokPerWarp; ++t)
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int ch = lane + 32 * (k0 + k);
-                if (ch < nchunk) {
-                    const float4 ma = *reinterpret_cast<const float4*>(m_s + ch * 8);
-                    const float4 mb = *reinterpret_cast<const float4*>(m_s + ch * 8 + 4);
-                    const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-                    const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+        for (int e = 0; e < 4; ++e) acc[t][e] = 0ull;
+    constexpr int kBatch = 4;                                           // chunks per token in flight
+    for (int k0 = 0; k0 < h1; k0 += kBatch) {
+        uint4 v[kTokPerWarp][kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const int ch = lane + 32 * (k0 + k);
+#pragma unroll
+            for (int t = 0; t < kTokPerWarp; ++t)
+                v[t][k] = (ch < nchunk && tv[t]) ? __ldg(rows[t] + ch) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const int ch = lane + 32 * (k0 + k);
+            if (ch < nchunk) {
+                const float4 ma = *reinterpret_cast<const float4*>(m_s + ch * 8);
+                const float4 mb = *reinterpret_cast<const float4*>(m_s + ch * 8 + 4);
+                const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+#pragma unroll
+                for (int t = 0; t < kTokPerWarp; ++t) {
+                    const uint32_t w[4] = {v[t][k].x, v[t][k].y, v[t][k].z, v[t][k].w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const uint64_t x2 = f2_pack(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xFFFF0000u));
                         const uint64_t d2 = f2_fma(f2_pack(mm[2 * e], mm[2 * e + 1]), neg1, x2);   // fl(x - m')
-                        acc[e] = f2_fma(d2, d2, acc[e]);
+                        acc[t][e] = f2_fma(d2, d2, acc[t][e]);
                     }
                 }
             }
         }
+    }
+    float sums[kTokPerWarp];
+#pragma unroll
+    for (int t = 0; t < kTokPerWarp; ++t) {
         float a[8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) f2_unpack(acc[e], a[2 * e], a[2 * e + 1]);
-        float s = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+        for (int e = 0; e < 4; ++e) f2_unpack(acc[t][e], a[2 * e], a[2 * e + 1]);
+        float sm = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        if (lane == 0) {
+        for (int off = 16; off > 0; off >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, off);
+        sums[t] = sm;
+    }
+    // lane t finishes token t of the warp: bound and outputs
+    if (lane < kTokPerWarp) {
+        const int i = blockIdx.x * kScoreTok + warp * kTokPerWarp + lane;
+        float s = sums[0];
+#pragma unroll
+        for (int t = 1; t < kTokPerWarp; ++t)
+            if (lane == t) s = sums[t];
+        if (i < N) {
             if (!(s >= 0.f) || isinf(s)) atomicCAS(status, 0, VAR_ERR_NUMERIC);   // nan / inf input
             const float e1 = __fmul_ru(c1, s);
             const float rs = __fsqrt_ru(__fmul_ru(s, __fadd_ru(1.f, __fmul_ru(2.f, c1))));
@@ -503,91 +481,357 @@ __global__ void __launch_bounds__(kScoreThreads)
             if (scores) scores[o] = s;
         }
     }
+}
 
-    // ---- the last CTA of batch element b selects
-    __threadfence();
+// ------------------------------------------------------------------ 3. select
+
+// Order-preserving map float -> uint32 (larger float -> larger key).
+__device__ __forceinline__ uint32_t f32_key(float f)
+{
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// fp64 score of one token in the exact evaluation order: lane l sums channels
+// [l*q, (l+1)*q) as a halving tree, the 32 lane sums are combined pairwise by
+// the xor butterfly (the top five levels of the same tree; C = 32 q).
+// Subtrees of 8 or fewer leaves whose size is a power of two are expanded at
+// compile time; above them the tree (split at n/2 rounded down) is walked
+// iteratively with a small explicit stack, so no recursion and little stack.
+template <int n>
+__device__ __forceinline__ double tree64_pow2(const __nv_bfloat16* x, const double* m)
+{
+    if constexpr (n == 1) {
+        const double d = __dsub_rn(static_cast<double>(__bfloat162float(x[0])), m[0]);
+        return __dmul_rn(d, d);
+    } else {
+        const double a = tree64_pow2<n / 2>(x, m);
+        const double bb = tree64_pow2<n / 2>(x + n / 2, m + n / 2);
+        return __dadd_rn(a, bb);
+    }
+}
+
+__device__ __forceinline__ bool tree64_leaf_block(const __nv_bfloat16* x, const double* m, int n, double& r)
+{
+    switch (n) {
+    case 1: r = tree64_pow2<1>(x, m); return true;
+    case 2: r = tree64_pow2<2>(x, m); return true;
+    case 4: r = tree64_pow2<4>(x, m); return true;
+    case 8: r = tree64_pow2<8>(x, m); return true;
+    default: return false;
+    }
+}
+
+__device__ __noinline__ double tree64(const __nv_bfloat16* x, const double* m, int n)
+{
+    constexpr int kDepth = 16;                 // n <= 2^15 leaves
+    int fs[kDepth], fn[kDepth], fst[kDepth];   // frame: start, size, state
+    double fl[kDepth];                         // frame: left subtree's sum
+    int sp = 0;
+    fs[0] = 0; fn[0] = n; fst[0] = 0; sp = 1;
+    double ret = 0.0;
+    while (sp > 0) {
+        const int t = sp - 1;
+        double leaf;
+        if (fst[t] == 0 && tree64_leaf_block(x + fs[t], m + fs[t], fn[t], leaf)) {
+            ret = leaf;
+            --sp;
+        } else if (fst[t] == 0) {              // descend left
+            fst[t] = 1;
+            fs[sp] = fs[t]; fn[sp] = fn[t] / 2; fst[sp] = 0; ++sp;
+        } else if (fst[t] == 1) {              // left done: descend right
+            fl[t] = ret;
+            fst[t] = 2;
+            fs[sp] = fs[t] + fn[t] / 2; fn[sp] = fn[t] - fn[t] / 2; fst[sp] = 0; ++sp;
+        } else {                               // both done
+            ret = __dadd_rn(fl[t], ret);
+            --sp;
+        }
+    }
+    return ret;
+}
+
+// Sum over threads with a larger index of v (exclusive suffix sum over the
+// CTA in thread order); every thread calls it.  wtmp: kSelWarps ints.
+__device__ __forceinline__ int block_suffix_excl(int v, int* wtmp)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int s = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_down_sync(0xffffffffu, s, off);
+        if (lane + off < 32) s += y;
+    }
     __syncthreads();
-    if (tid == 0) is_last = atomicAdd(&counters[b], 1) == static_cast<int>(gridDim.x) - 1;
+    if (lane == 0) wtmp[warp] = s;
     __syncthreads();
-    if (!is_last || K == 0) return;
-    __threadfence();
+    int t = (lane > warp && lane < kSelWarps) ? wtmp[lane] : 0;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+    return t + s - v;
+}
+
+// Sum over threads with a smaller index of v (exclusive prefix sum); every
+// thread calls it; *total receives the sum over the CTA.
+__device__ __forceinline__ int block_prefix_excl(int v, int* wtmp, int* total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int s = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, s, off);
+        if (lane >= off) s += y;
+    }
+    __syncthreads();
+    if (lane == 31) wtmp[warp] = s;
+    __syncthreads();
+    int t = (lane < warp) ? wtmp[lane] : 0;
+    int all = wtmp[lane];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        t += __shfl_xor_sync(0xffffffffu, t, off);
+        all += __shfl_xor_sync(0xffffffffu, all, off);
+    }
+    *total = all;
+    return t + s - v;
+}
+
+struct SelShared {
+    int hist[2][kSelBins];
+    uint32_t cand[2][kSelCand];
+    int wtmp[kSelWarps];
+    int blk[kMaxKeysPerThread * kSelWarps];   // per (k, warp) block: packed counts, then offsets
+    uint32_t red[4][kSelWarps];
+    uint32_t lo[2], hi[2];                 // narrowing state per side: inclusive key range,
+    int want[2], cnt[2], done[2], ncand[2];   // the answer's rank in it, keys in it
+    uint32_t res[2];
+    uint8_t keep_band[kMaxN];              // band tokens kept after the fp64 re-score
+};
+
+// The r0-th largest of side 0's keys and the r1-th largest of side 1's keys
+// (1-based; equal keys count separately).  Token i = tid + kSelThreads*k holds
+// k0[k], k1[k] when i < n.  Each side keeps an inclusive key range holding its
+// answer; a level histograms the range into power-of-two bins and keeps the bin
+// where the descending count reaches the rank; a range of at most kSelCand keys
+// is ranked by brute force.
+template <int KPT>
+__device__ void dual_kth_largest(const uint32_t (&k0)[KPT], const uint32_t (&k1)[KPT],
+                                 int n, int r0, int r1, SelShared& S, uint32_t& out0, uint32_t& out1)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t mn0 = 0xFFFFFFFFu, mx0 = 0u, mn1 = 0xFFFFFFFFu, mx1 = 0u;
+#pragma unroll
+    for (int k = 0; k < KPT; ++k) {
+        if (tid + kSelThreads * k < n) {
+            mn0 = min(mn0, k0[k]); mx0 = max(mx0, k0[k]);
+            mn1 = min(mn1, k1[k]); mx1 = max(mx1, k1[k]);
+        }
+    }
+    mn0 = __reduce_min_sync(0xffffffffu, mn0);
+    mx0 = __reduce_max_sync(0xffffffffu, mx0);
+    mn1 = __reduce_min_sync(0xffffffffu, mn1);
+    mx1 = __reduce_max_sync(0xffffffffu, mx1);
+    if (lane == 0) {
+        S.red[0][warp] = mn0; S.red[1][warp] = mx0; S.red[2][warp] = mn1; S.red[3][warp] = mx1;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t a = __reduce_min_sync(0xffffffffu, S.red[0][lane]);
+        const uint32_t bq = __reduce_max_sync(0xffffffffu, S.red[1][lane]);
+        const uint32_t c = __reduce_min_sync(0xffffffffu, S.red[2][lane]);
+        const uint32_t d = __reduce_max_sync(0xffffffffu, S.red[3][lane]);
+        if (lane == 0) {
+            S.lo[0] = a; S.hi[0] = bq; S.lo[1] = c; S.hi[1] = d;
+            S.want[0] = r0; S.want[1] = r1;
+            S.cnt[0] = S.cnt[1] = n;
+            S.done[0] = S.done[1] = 0;
+        }
+    }
+    __syncthreads();
+    for (int level = 0; level < 8; ++level) {
+        // this level's state, read by every thread before anyone updates it;
+        // mode per side: 0 done, 1 histogram, 2 brute force
+        int mode[2], shift[2], want[2];
+        uint32_t rlo[2], rhi[2];
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            rlo[s] = S.lo[s];
+            rhi[s] = S.hi[s];
+            want[s] = S.want[s];
+            mode[s] = S.done[s] ? 0 : (rlo[s] == rhi[s] ? 0 : (S.cnt[s] <= kSelCand ? 2 : 1));
+            const uint32_t span_m1 = rhi[s] - rlo[s];            // span - 1
+            const int bits = span_m1 ? 32 - __clz(static_cast<int>(span_m1)) : 0;   // span <= 2^bits
+            shift[s] = max(0, bits - 11);
+        }
+        if (S.done[0] && S.done[1]) break;
+        __syncthreads();
+        if (tid == 0) {
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                if (!S.done[s] && rlo[s] == rhi[s]) { S.res[s] = rlo[s]; S.done[s] = 1; }
+                S.ncand[s] = 0;
+            }
+        }
+        if (mode[0] == 1 || mode[1] == 1)
+            for (int j = tid; j < 2 * kSelBins; j += kSelThreads) (&S.hist[0][0])[j] = 0;
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < KPT; ++k) {
+            if (tid + kSelThreads * k >= n) continue;
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                const uint32_t key = s ? k1[k] : k0[k];
+                if (!mode[s] || key < rlo[s] || key > rhi[s]) continue;
+                if (mode[s] == 1) {
+                    atomicAdd(&S.hist[s][(key - rlo[s]) >> shift[s]], 1);
+                } else {
+                    const int j = atomicAdd(&S.ncand[s], 1);
+                    S.cand[s][j] = key;
+                }
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            if (mode[s] == 2) {
+                const int nc = S.ncand[s];
+                for (int t = tid; t < nc; t += kSelThreads) {
+                    const uint32_t v = S.cand[s][t];
+                    int g = 0, e = 0;
+                    for (int u = 0; u < nc; ++u) {
+                        const uint32_t w = S.cand[s][u];
+                        g += w > v;
+                        e += w == v;
+                    }
+                    if (g < want[s] && want[s] <= g + e) { S.res[s] = v; S.done[s] = 1; }
+                }
+            } else if (mode[s] == 1) {
+                // thread t owns bins [2t, 2t + 2); count the keys in higher bins
+                const int c_lo = S.hist[s][2 * tid], c_hi = S.hist[s][2 * tid + 1];
+                const int above = block_suffix_excl(c_lo + c_hi, S.wtmp);
+                const int cnts[2] = {c_hi, c_lo};
+                int ab = above;
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int cc = cnts[u];
+                    if (ab < want[s] && want[s] <= ab + cc) {
+                        const uint32_t bin = static_cast<uint32_t>(2 * tid + 1 - u);
+                        const uint32_t lo = rlo[s] + (bin << shift[s]);
+                        const uint32_t w1 = (1u << shift[s]) - 1u;
+                        S.want[s] = want[s] - ab;
+                        S.cnt[s] = cc;
+                        S.lo[s] = lo;
+                        S.hi[s] = lo + min(w1, rhi[s] - lo);
+                    }
+                    ab += cc;
+                }
+            }
+        }
+        __syncthreads();
+    }
+    out0 = S.res[0];
+    out1 = S.res[1];
+}
+
+template <int KPT>
+__global__ void __launch_bounds__(kSelThreads, 1)
+    pivot_select_kernel(const __nv_bfloat16* __restrict__ x, int N, int C, int K, const float* __restrict__ lo_g,
+                        const float* __restrict__ hi_g, const double* __restrict__ mean64,
+                        int* __restrict__ band_idx_g, double* __restrict__ band_score_g,
+                        int32_t* __restrict__ idx_out, int32_t* status)
+{
+    __shared__ SelShared S;
+    const int b = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_wait();   // the scores of the score kernel
     int32_t* out = idx_out + static_cast<size_t>(b) * K;
     if (K == N) {
-        for (int j = tid; j < N; j += kScoreThreads) out[j] = j;
+        for (int j = tid; j < N; j += kSelThreads) out[j] = j;
         return;
     }
-    for (int j = tid; j < N; j += kScoreThreads) {
-        klo[j] = f32_key(__ldcg(lo_g + static_cast<size_t>(b) * N + j));
-        khi[j] = f32_key(__ldcg(hi_g + static_cast<size_t>(b) * N + j));
+    uint32_t ka[KPT], kh[KPT];
+#pragma unroll
+    for (int k = 0; k < KPT; ++k) {
+        const int i = tid + kSelThreads * k;
+        ka[k] = kh[k] = 0u;
+        if (i < N) {
+            ka[k] = f32_key(__ldcg(lo_g + static_cast<size_t>(b) * N + i));
+            kh[k] = f32_key(__ldcg(hi_g + static_cast<size_t>(b) * N + i));
+        }
+    }
+    uint32_t t_lo, t_hi;
+    dual_kth_largest(ka, kh, N, K, K + 1, S, t_lo, t_hi);
+
+    // classify: 1 certainly kept, 2 band, 0 certainly dropped.  Block (k, w) =
+    // the 32 consecutive tokens kSelThreads*k + 32w + [0, 32) held by warp w,
+    // so blocks in (k, w) order are in token order.
+    uint32_t fin = 0u, fband = 0u;    // bit k: token k of this thread kept / in the band
+#pragma unroll
+    for (int k = 0; k < KPT; ++k) {
+        if (tid + kSelThreads * k < N) {
+            if (ka[k] > t_hi) fin |= 1u << k;
+            else if (!(kh[k] < t_lo)) fband |= 1u << k;
+        }
+    }
+    const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int k = 0; k < KPT; ++k) {
+        const int ci = __popc(__ballot_sync(0xffffffffu, (fin >> k) & 1u));
+        const int cb = __popc(__ballot_sync(0xffffffffu, (fband >> k) & 1u));
+        if (lane == 0) S.blk[k * kSelWarps + warp] = (ci << 16) | cb;
     }
     __syncthreads();
-    uint32_t t_lo, t_hi;
-    dual_radix_select(klo, K, khi, K + 1, N, hist, sel, t_lo, t_hi);
-
-    // classify (1 certainly kept, 2 band, 0 certainly dropped); warp w owns a
-    // contiguous range of tokens, so ballots keep the output ascending
-    const int per_warp = ((N + kScoreWarps - 1) / kScoreWarps + 31) & ~31;
-    const int w0 = min(N, warp * per_warp), w1 = min(N, w0 + per_warp);
-    int n_in = 0, n_band = 0;
-    for (int i0 = w0; i0 < w1; i0 += 32) {
-        const int i = i0 + lane;
-        int f = 0;
-        if (i < w1) {
-            f = klo[i] > t_hi ? 1 : (khi[i] < t_lo ? 0 : 2);
-            flg[i] = static_cast<uint8_t>(f);
-        }
-        n_in += __popc(__ballot_sync(0xffffffffu, f == 1));
-        n_band += __popc(__ballot_sync(0xffffffffu, f == 2));
+    // offsets of the blocks: thread j < KPT*kSelWarps owns block j
+    int tot;
+    {
+        const int v = tid < KPT * kSelWarps ? S.blk[tid] : 0;
+        const int off = block_prefix_excl(v, S.wtmp, &tot);
+        __syncthreads();
+        if (tid < KPT * kSelWarps) S.blk[tid] = off;
+        __syncthreads();
     }
-    int tot_in, tot_band;
-    const int off_in = warp_offsets(n_in, wsc, &tot_in);
-    const int off_band = warp_offsets(n_band, wsc, &tot_band);
+    const int tot_in = tot >> 16, tot_band = tot & 0xFFFF;
     const int need = K - tot_in;
     if (need < 0 || need > tot_band) {
         if (tid == 0) atomicCAS(status, 0, VAR_ERR_NUMERIC);
         return;
     }
-    const uint32_t lt = (1u << lane) - 1u;
     if (need == 0 || need == tot_band) {
         // the band is decided by count alone
         const bool keep_band = need > 0;
-        int pos = off_in + (keep_band ? off_band : 0);
-        for (int i0 = w0; i0 < w1; i0 += 32) {
-            const int i = i0 + lane;
-            const int f = i < w1 ? flg[i] : 0;
-            const bool kept = f == 1 || (f == 2 && keep_band);
-            const uint32_t m = __ballot_sync(0xffffffffu, kept);
-            if (kept) out[pos + __popc(m & lt)] = i;
-            pos += __popc(m);
+#pragma unroll
+        for (int k = 0; k < KPT; ++k) {
+            const int off = S.blk[k * kSelWarps + warp];
+            const bool kept = ((fin >> k) & 1u) || (keep_band && ((fband >> k) & 1u));
+            const uint32_t mi = __ballot_sync(0xffffffffu, (fin >> k) & 1u);
+            const uint32_t mb = __ballot_sync(0xffffffffu, (fband >> k) & 1u);
+            const uint32_t m = keep_band ? (mi | mb) : mi;
+            const int pos = (off >> 16) + (keep_band ? (off & 0xFFFF) : 0) + __popc(m & lt);
+            if (kept) out[pos] = tid + kSelThreads * k;
         }
         return;
     }
     // fp64 re-score of the band in the exact evaluation order
     int* band_idx = band_idx_g + static_cast<size_t>(b) * N;
     double* band_score = band_score_g + static_cast<size_t>(b) * N;
-    {
-        int pos = off_band;
-        for (int i0 = w0; i0 < w1; i0 += 32) {
-            const int i = i0 + lane;
-            const bool inb = i < w1 && flg[i] == 2;
-            const uint32_t m = __ballot_sync(0xffffffffu, inb);
-            if (inb) band_idx[pos + __popc(m & lt)] = i;
-            pos += __popc(m);
-        }
+#pragma unroll
+    for (int k = 0; k < KPT; ++k) {
+        const uint32_t mb = __ballot_sync(0xffffffffu, (fband >> k) & 1u);
+        if ((fband >> k) & 1u) band_idx[(S.blk[k * kSelWarps + warp] & 0xFFFF) + __popc(mb & lt)] = tid + kSelThreads * k;
     }
     __syncthreads();
     const int q = C / 32;
-    const double* mb = mean64 + static_cast<size_t>(b) * C;
-    for (int j = warp; j < tot_band; j += kScoreWarps) {
+    const double* mb64 = mean64 + static_cast<size_t>(b) * C;
+    for (int j = warp; j < tot_band; j += kSelWarps) {
         const int i = band_idx[j];
         const __nv_bfloat16* row = x + (static_cast<size_t>(b) * N + i) * C;
-        double v = tree64(row + lane * q, mb + lane * q, q);
+        double v = tree64(row + lane * q, mb64 + lane * q, q);
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) v = __dadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
         if (lane == 0) band_score[j] = v;
     }
     __syncthreads();
-    for (int j = tid; j < tot_band; j += kScoreThreads) {
+    for (int j = tid; j < tot_band; j += kSelThreads) {
         const double sj = band_score[j];
         const int ij = band_idx[j];
         int better = 0;
@@ -595,29 +839,33 @@ __global__ void __launch_bounds__(kScoreThreads)
             const double st = band_score[t];
             better += (st > sj) || (st == sj && band_idx[t] < ij);
         }
-        flg[ij] = better < need ? 1 : 0;
+        S.keep_band[ij] = better < need ? 1 : 0;
     }
     __syncthreads();
-    int n_sel = 0;
-    for (int i0 = w0; i0 < w1; i0 += 32) {
-        const int i = i0 + lane;
-        n_sel += __popc(__ballot_sync(0xffffffffu, i < w1 && flg[i] == 1));
+    uint32_t fsel = fin;
+#pragma unroll
+    for (int k = 0; k < KPT; ++k)
+        if (((fband >> k) & 1u) && S.keep_band[tid + kSelThreads * k]) fsel |= 1u << k;
+#pragma unroll
+    for (int k = 0; k < KPT; ++k) {
+        const int cs = __popc(__ballot_sync(0xffffffffu, (fsel >> k) & 1u));
+        if (lane == 0) S.blk[k * kSelWarps + warp] = cs;
     }
-    int tot_sel;
-    int pos = warp_offsets(n_sel, wsc, &tot_sel);
-    if (tid == 0 && tot_sel != K) atomicCAS(status, 0, VAR_ERR_NUMERIC);
-    for (int i0 = w0; i0 < w1; i0 += 32) {
-        const int i = i0 + lane;
-        const bool kept = i < w1 && flg[i] == 1;
-        const uint32_t m = __ballot_sync(0xffffffffu, kept);
-        if (kept && pos + __popc(m & lt) < K) out[pos + __popc(m & lt)] = i;
-        pos += __popc(m);
+    __syncthreads();
+    {
+        const int v = tid < KPT * kSelWarps ? S.blk[tid] : 0;
+        const int off = block_prefix_excl(v, S.wtmp, &tot);
+        __syncthreads();
+        if (tid < KPT * kSelWarps) S.blk[tid] = off;
+        __syncthreads();
     }
-}
-
-size_t score_smem_bytes(int N, int C)
-{
-    return ((static_cast<size_t>(C) * 4 + 15) & ~size_t(15)) + static_cast<size_t>(N) * 9;
+    if (tid == 0 && tot != K) atomicCAS(status, 0, VAR_ERR_NUMERIC);
+#pragma unroll
+    for (int k = 0; k < KPT; ++k) {
+        const uint32_t m = __ballot_sync(0xffffffffu, (fsel >> k) & 1u);
+        const int pos = S.blk[k * kSelWarps + warp] + __popc(m & lt);
+        if (((fsel >> k) & 1u) && pos < K) out[pos] = tid + kSelThreads * k;
+    }
 }
 
 }  // namespace
@@ -629,8 +877,7 @@ int launch_pivot_select(int B, int N, int C, const void* xv, int keep_k, int32_t
 {
     const PivotWs w = pivot_ws_layout(B, N, C);
     if (ws_bytes < w.total) return VAR_ERR_WORKSPACE;
-    const size_t smem = score_smem_bytes(N, C);
-    if (smem > kScoreSmemMax) return VAR_ERR_UNSUPPORTED;
+    if (N > kMaxN || C > 16384) return VAR_ERR_UNSUPPORTED;
     int32_t* status = device_status_ptr();
     if (!status) return VAR_ERR_CUDA;
     int dev = 0;
@@ -640,8 +887,10 @@ int launch_pivot_select(int B, int N, int C, const void* xv, int keep_k, int32_t
         static bool attr[64] = {};
         std::lock_guard<std::mutex> lk(mu);
         if (!attr[dev]) {
-            if (cudaFuncSetAttribute(pivot_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kScoreSmemMax) != cudaSuccess)
+            if (cudaFuncSetAttribute(pivot_colsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kRingBytes) != cudaSuccess ||
+                cudaFuncSetAttribute(pivot_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     16384 * 4) != cudaSuccess)
                 return VAR_ERR_CUDA;
             attr[dev] = true;
         }
@@ -653,28 +902,45 @@ int launch_pivot_select(int B, int N, int C, const void* xv, int keep_k, int32_t
     auto* hik = reinterpret_cast<float*>(base + w.hik);
     auto* bidx = reinterpret_cast<int*>(base + w.band_idx);
     auto* bsc = reinterpret_cast<double*>(base + w.band_score);
-    auto* cnt = reinterpret_cast<int*>(base + w.counters);
     const auto* x = static_cast<const __nv_bfloat16*>(xv);
 
     {
         const dim3 grid(kSlabs, (C + kChunk - 1) / kChunk, B);
-        pivot_colsum_kernel<<<grid, kSumThreads, 0, st>>>(x, N, C, m64, m32, cnt, status);
+        pivot_colsum_kernel<<<grid, kSumThreads, kRingBytes, st>>>(x, N, C, m64, m32, status);
         if (cudaGetLastError() != cudaSuccess) return VAR_ERR_CUDA;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((N + kScoreTok - 1) / kScoreTok, B, 1);
-    cfg.blockDim = dim3(kScoreThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, pivot_score_kernel, x, N, C, keep_k,
-                                             static_cast<const float*>(m32), static_cast<const double*>(m64),
-                                             lok, hik, scores, cnt, bidx, bsc, idx, status);
-    return cuda_status(e);
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((N + kScoreTok - 1) / kScoreTok, B, 1);
+        cfg.blockDim = dim3(kScoreThreads, 1, 1);
+        cfg.dynamicSmemBytes = static_cast<size_t>(C) * 4;
+        cfg.stream = st;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, pivot_score_kernel, x, N, C, static_cast<const float*>(m32), lok, hik, scores,
+                               status) != cudaSuccess)
+            return VAR_ERR_CUDA;
+    }
+    if (keep_k > 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(B, 1, 1);
+        cfg.blockDim = dim3(kSelThreads, 1, 1);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = st;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        auto* fn = N <= 4 * kSelThreads ? pivot_select_kernel<4>
+                   : N <= 8 * kSelThreads ? pivot_select_kernel<8>
+                                          : pivot_select_kernel<kMaxKeysPerThread>;
+        if (cudaLaunchKernelEx(&cfg, fn, x, N, C, keep_k, static_cast<const float*>(lok),
+                               static_cast<const float*>(hik), static_cast<const double*>(m64), bidx, bsc, idx,
+                               status) != cudaSuccess)
+            return VAR_ERR_CUDA;
+    }
+    return VAR_OK;
 }
 
 // ---------------------------------------------------------------------------
@@ -732,7 +998,7 @@ extern "C" int var_pivot_select_noalloc(const var_problem* p, int32_t step, cons
     uint8_t* ws = pivot_scratch_ptr();
     if (!ws) return VAR_ERR_CUDA;
     // Nothing in the scratch needs clearing: every word is written before it
-    // is read within a call (the colsum kernel resets the per-batch counters).
+    // is read within a call.
     return launch_pivot_select(B, N, channels, x, keep_k, idx, scores, ws, kNoAllocBytes,
                                static_cast<cudaStream_t>(stream));
 }
