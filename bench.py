@@ -1,17 +1,26 @@
 #!/usr/bin/env python3
 """Benchmark of the next-scale VAR attention hot path on B300.
 
-Headline (one JSON line on rank 0): final-scale attention of the 1024px
-schedule -- 4,096 queries (64x64 grid) of a CFG pair (batch 2), 16 heads,
-head_dim 128, attending a 10,521-token cache -- in ms and TFLOP/s through the
-C ABI (var_attn_dense), with:
-  roofline      the attention kernel against the measured dense bf16 peak
-  e2e           the same call with host buffers (pinned H2D of Q/K/V and D2H
-                of O inside the timed region)
-  rows          every other hot-path kernel on its own workload's final scale
-                (pivot select + pruned attention + restore at 64x64 r=0.2;
-                block-sparse attention of the 2K schedule), each timed alone
-  cpu_baseline  the fp64 CPU oracle on a bounded sample of the same workload
+One step = the final scale of the 1024px schedule (64x64 = 4,096 queries of a
+CFG pair, 16 heads, head_dim 128, attending a 10,521-token cache) taken
+through every row of the hot path, all through the C ABI:
+  dense attention      var_attn_dense
+  pivot selection      var_pivot_select      (hidden states 4096 x 2048, keep 20 %)
+  pruned attention     var_attn_pruned
+  restore + scatter    var_restore_scatter   (from the 48x48 step's output)
+  block-sparse         var_attn_blocksparse  (sinks <= 16, +-2 block window;
+                                              the mask is built once on the host)
+`value` is the step's dense-equivalent TFLOP/s: the dense FLOPs of the three
+attention variants (each computes the final-scale attention) divided by the
+step time.  The JSON line also carries:
+  rows          per-kernel times inside the timed region (CUDA events between
+                the calls) and separate measurements: the small kernels from a
+                CUDA graph after an L2 flush, the 2K block-sparse workload, the
+                256px schedule
+  roofline      the step's dominant kernel against the measured peak
+  e2e           the same step with host buffers (pinned H2D of its inputs, D2H
+                of its outputs, inside the timed region)
+  cpu_baseline  the fp64 CPU oracle on a bounded sample of the same work
   clocks        SM clock and throttle reasons sampled during the timed region
 
 `--impl reference` times the CPU oracle as the reference arm.
@@ -40,7 +49,12 @@ import torch  # noqa: E402
 from var_synth import WORKLOADS, cache_len, make_inputs  # noqa: E402
 
 METRIC = "final-scale attention ms and TFLOP/s (dense-equiv) at 1 B300; % of BF16 peak"
-HEADLINE = "dense_1024px"
+STEP_WORKLOAD = "pruned_1024px"      # tensors of the 1024px schedule (CFG pair, sink) + hidden states
+FINAL = 12                           # the 64x64 step
+KEEP = (1, 5)                        # keep ratio at 64x64
+QBLOCK, RADIUS, SINK_SIDE = 8, 2, 16
+ROW_NAMES = ("attn_dense", "pivot_select", "attn_pruned", "restore_scatter", "attn_blocksparse")
+LAUNCHES_PER_STEP = 7                # dense 1, pivot 3, pruned 1, restore 1, block-sparse 1
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -85,17 +99,17 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str, units: float):
-    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, scaled
-    to `units` of work, or None when absent or taken on other kernel sources."""
+def ncu_traffic(key: str):
+    """Per-launch DRAM bytes (read + write) of a kernel on a workload from the
+    committed ncu summary, or None when absent or taken on other kernel sources."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
     d = json.load(open(path))
-    e = d.get(kernel)
+    e = d.get(key)
     if not e or e.get("source_hash") != kernel_source_hash():
         return None
-    return e["dram_bytes"] * units / e["units"]
+    return e["dram_bytes"]
 
 
 class ClockSampler:
@@ -156,27 +170,145 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def time_loop(fn, steps: int, stream) -> float:
-    """Mean ms per call of fn() over `steps` calls, CUDA events on `stream`."""
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
+def flops_attn(B, H, Nq, Lk, D) -> float:
+    """QK^T and PV: 4 D FLOPs per (query, key) pair."""
+    return 4.0 * B * H * Nq * Lk * D
+
+
+def mask_kept_pairs(sides, row_ptr, entries, sink_len, qblock) -> int:
+    """(query, key) pairs a block mask keeps, counted from its CSR."""
+    pairs = 0
+    for qb in range(len(row_ptr) - 1):
+        nk = sink_len
+        for e in entries[row_ptr[qb]:row_ptr[qb + 1]]:
+            sc, u, vv = int(e) >> 24, (int(e) >> 12) & 0xFFF, int(e) & 0xFFF
+            s = sides[sc]
+            nk += (min(s, u * qblock + qblock) - u * qblock) * (min(s, vv * qblock + qblock) - vv * qblock)
+        pairs += nk * qblock * qblock
+    return pairs
+
+
+class L2Flush:
+    """Evicts L2 by reading a buffer twice its size (reads leave no dirty lines)."""
+
+    def __init__(self, dev):
+        self.buf = torch.zeros(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.buf.sum()
+
+
+def time_graph(fn, iters: int, flush: L2Flush) -> float:
+    """Median ms of one fn() replayed from a CUDA graph, L2 flushed before each replay."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()                                   # warm up on the capture stream
+    torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(steps):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
         fn()
-    e1.record(stream)
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / steps
+    ts = []
+    for _ in range(iters):
+        flush()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+# ----------------------------------------------------------------------------- the step
+
+class Step:
+    """Device buffers and the call sequence of one step."""
+
+    def __init__(self, V, dev, inp):
+        w = WORKLOADS[STEP_WORKLOAD]
+        self.V = V
+        self.w = w
+        B, H, D = w.batch, w.heads, w.head_dim
+        self.p = V.problem(B, H, D, w.sides, kv_capacity=inp.k.shape[2])
+        self.N = w.sides[FINAL] ** 2
+        self.L = cache_len(w.sides, FINAL)
+        self.K = V.var_keep_count(self.N, *KEEP)
+        self.q = inp.q[FINAL].to(dev)
+        self.k = inp.k.to(dev)
+        self.v = inp.v.to(dev)
+        self.x = inp.x[FINAL].to(dev)
+        self.C = self.x.shape[2]
+        # the previous (48x48) step's output: dense attention, computed once
+        q11 = inp.q[FINAL - 1].to(dev)
+        self.prev = torch.empty_like(q11)
+        V.var_attn_dense(self.p, FINAL - 1, q11, self.k, self.v, self.prev)
+        del q11
+        self.o_dense = torch.empty_like(self.q)
+        self.ws = torch.empty(V.var_pivot_workspace_bytes(self.p, FINAL, self.C), dtype=torch.uint8, device=dev)
+        self.idx = torch.empty((B, self.K), dtype=torch.int32, device=dev)
+        self.oc = torch.empty((B, H, self.K, D), dtype=torch.bfloat16, device=dev)
+        self.o_pruned = torch.empty_like(self.q)
+        self.o_sparse = torch.empty_like(self.q)
+        t0 = time.perf_counter()
+        rp, en, sink = V.var_block_mask_build(self.p, FINAL, QBLOCK, RADIUS, SINK_SIDE)
+        self.mask_build_ms = (time.perf_counter() - t0) * 1e3
+        self.rp = torch.as_tensor(rp, device=dev)
+        self.en = torch.as_tensor(en, device=dev)
+        self.mask = V.block_mask_struct(QBLOCK, self.rp, self.en, sink)
+        self.sparse_pairs = mask_kept_pairs(w.sides, rp, en, sink, QBLOCK)
+        self.flops_dense = flops_attn(B, H, self.N, self.L, D)
+        self.flops_pruned = flops_attn(B, H, self.K, self.L, D)
+        self.flops_sparse = 4.0 * B * H * self.sparse_pairs * D
+        self.bytes_pivot = self.x.numel() * 2 + self.idx.numel() * 4
+        self.bytes_restore = (self.prev.numel() + self.oc.numel() + self.o_pruned.numel()) * 2 + self.idx.numel() * 4
+
+    def calls(self, stream=None):
+        V, p = self.V, self.p
+        return (
+            lambda: V.var_attn_dense(p, FINAL, self.q, self.k, self.v, self.o_dense, stream=stream),
+            lambda: V.var_pivot_select(p, FINAL, self.x, self.K, self.idx, self.ws, stream=stream),
+            lambda: V.var_attn_pruned(p, FINAL, self.q, self.k, self.v, self.idx, self.K, self.oc, stream=stream),
+            lambda: V.var_restore_scatter(p, FINAL, self.prev, self.oc, self.idx, self.K, self.o_pruned,
+                                          stream=stream),
+            lambda: V.var_attn_blocksparse(p, FINAL, self.q, self.k, self.v, self.mask, self.o_sparse,
+                                           stream=stream),
+        )
+
+    def run(self, stream=None):
+        for c in self.calls(stream):
+            c()
+
+
+def time_step(step: Step, steps: int, stream):
+    """Total ms per step and per-row ms, CUDA events on `stream` between the calls."""
+    calls = step.calls(stream)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for s in range(steps):
+        ev[s][0].record(stream)
+        for i, c in enumerate(calls):
+            c()
+            ev[s][i + 1].record(stream)
+    torch.cuda.synchronize()
+    total = ev[0][0].elapsed_time(ev[-1][-1]) / steps
+    per_row = [sum(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(steps)) / steps for i in range(len(calls))]
+    return total, per_row
 
 
 # ----------------------------------------------------------------------------- CPU oracle arm
 
-def oracle_calibrate(w, inp, step, budget_s: float):
-    """Number of query rows of `step` the oracle computes in about budget_s."""
+def oracle_sample(inp, budget_s: float, seed: int = 0):
+    """Time the oracle on random query rows of the final step's dense attention,
+    sized to about budget_s: (TFLOP/s, seconds, rows, threads)."""
     import oracle
-    q = inp.q[step]
+    w = WORKLOADS[STEP_WORKLOAD]
+    q = inp.q[FINAL]
     B, H, N, D = q.shape
-    L = cache_len(w.sides, step)
+    L = cache_len(w.sides, FINAL)
     oracle.attention(q, inp.k, inp.v, L, rows=np.arange(2))        # load + warm
     n = 8
     while True:
@@ -184,51 +316,47 @@ def oracle_calibrate(w, inp, step, budget_s: float):
         oracle.attention(q, inp.k, inp.v, L, rows=np.arange(n) * (B * H * N // n))
         dt = time.perf_counter() - t0
         if dt >= 0.25 * budget_s or n >= B * H * N:
-            return int(max(1, min(B * H * N, n * budget_s / max(dt, 1e-6))))
+            break
         n = min(B * H * N, 4 * n)
-
-
-def oracle_run(w, inp, step, n_rows: int, seed: int = 0):
-    """Time the oracle on n_rows random query rows of `step`: (TFLOP/s, s, threads)."""
-    import oracle
-    q = inp.q[step]
-    B, H, N, D = q.shape
-    L = cache_len(w.sides, step)
+    n_rows = int(max(1, min(B * H * N, n * budget_s / max(dt, 1e-6))))
     rows = np.sort(np.random.default_rng(seed).choice(B * H * N, size=n_rows, replace=False))
     t0 = time.perf_counter()
     oracle.attention(q, inp.k, inp.v, L, rows=rows)
     dt = time.perf_counter() - t0
-    return n_rows * 4.0 * L * D / dt / 1e12, dt, oracle.num_threads()
+    return n_rows * 4.0 * L * D / dt / 1e12, dt, n_rows, oracle.num_threads()
+
+
+def step_config(inp):
+    w = WORKLOADS[STEP_WORKLOAD]
+    q = inp.q[FINAL]
+    B, H, N, D = q.shape
+    return {"workload": "final_step_1024px", "schedule": list(w.sides), "batch": B, "heads": H,
+            "head_dim": D, "queries": N, "keys": cache_len(w.sides, FINAL), "channels": w.channels,
+            "keep": f"{KEEP[0]}/{KEEP[1]}", "block_mask": f"qblock {QBLOCK}, radius {RADIUS}, sinks <= {SINK_SIDE}",
+            "rows": list(ROW_NAMES)}
 
 
 def run_reference(args):
     ws, rank, _ = dist_info()
     if rank != 0:
         return 0
-    w = WORKLOADS[args.workload]
-    step = w.steps[-1]
-    inp = make_inputs(w, steps=(step,))
+    inp = make_inputs(WORKLOADS[STEP_WORKLOAD], steps=(FINAL,))
     per_step = min(args.ref_seconds, 150.0 / (args.steps + args.warmup))
-    n_rows = oracle_calibrate(w, inp, step, per_step)
     vals = []
     for i in range(args.warmup + args.steps):
-        tf, dt, thr = oracle_run(w, inp, step, n_rows, seed=i)
+        tf, dt, n_rows, thr = oracle_sample(inp, per_step, seed=i)
         if i >= args.warmup:
             vals.append((tf, dt))
     value = statistics.median(v for v, _ in vals)
     ms = statistics.median(dt for _, dt in vals) * 1e3
-    q = inp.q[step]
-    B, H, N, D = q.shape
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic",
-        "config": {"workload": w.name, "batch": B, "heads": H, "head_dim": D, "queries": N,
-                   "keys": cache_len(w.sides, step)},
+        "data": "synthetic", "config": step_config(inp),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
-                         "sample": f"{n_rows} random query rows of the final step per step "
-                                   f"(of {B * H * N}); throughput scaled per FLOP"},
+                         "sample": f"{n_rows} random query rows of the final step's dense attention "
+                                   "per step; throughput per FLOP"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -237,96 +365,71 @@ def run_reference(args):
 
 # ----------------------------------------------------------------------------- GPU arm
 
-def bench_rows(V, dev, stream, steps: int):
-    """Time every non-headline kernel of the hot path on its own workload."""
+def extra_rows(V, dev, step: Step, iters: int, peaks):
+    """Separate measurements: small kernels alone, the 2K block-sparse workload,
+    the 256px schedule."""
     rows = {}
-    peaks = load_peaks()
-    # --- pruned final step of the 1024px schedule: pivot + pruned attention + restore
-    w = WORKLOADS["pruned_1024px"]
-    inp = make_inputs(w, steps=(11, 12))
-    B, H, D = w.batch, w.heads, w.head_dim
-    p = V.problem(B, H, D, w.sides)
-    step = 12
-    x = inp.x[step].to(dev)
-    N, Cc = x.shape[1], x.shape[2]
-    K = V.var_keep_count(N, 1, 5)
-    q = inp.q[step].to(dev)
-    k, v = inp.k.to(dev), inp.v.to(dev)
-    prev = torch.randn((B, H, 48 * 48, D), generator=torch.Generator().manual_seed(9)).to(torch.bfloat16).to(dev)
-    wsb = torch.empty(V.var_pivot_workspace_bytes(p, step, Cc), dtype=torch.uint8, device=dev)
-    idx = torch.empty((B, K), dtype=torch.int32, device=dev)
-    oc = torch.empty((B, H, K, D), dtype=torch.bfloat16, device=dev)
-    out = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=dev)
-    L = cache_len(w.sides, step)
-
-    def piv():
-        V.var_pivot_select(p, step, x, K, idx, wsb, stream=stream)
-
-    def pru():
-        V.var_attn_pruned(p, step, q, k, v, idx, K, oc, stream=stream)
-
-    def res():
-        V.var_restore_scatter(p, step, prev, oc, idx, K, out, stream=stream)
-
-    for f in (piv, pru, res):
-        for _ in range(3):
-            f()
-    t_piv = time_loop(piv, steps, stream)
-    t_pru = time_loop(pru, steps, stream)
-    t_res = time_loop(res, steps, stream)
-    fl_pru = 4.0 * B * H * K * L * D
-    fl_dense_eq = 4.0 * B * H * N * L * D
-    piv_bytes = x.numel() * 2 + B * K * 4
-    res_bytes = (prev.numel() + oc.numel() + out.numel()) * 2 + B * K * 4
-    rows["pivot_select_64x64"] = {"ms": t_piv, "bytes": piv_bytes, "GB/s": piv_bytes / t_piv / 1e6,
-                                  "frac_hbm": piv_bytes / t_piv / 1e6 / peaks["hbm_gbs"]}
-    rows["attn_pruned_64x64_r0.2"] = {"ms": t_pru, "TFLOP/s": fl_pru / t_pru / 1e9,
-                                      "frac_tensor": fl_pru / t_pru / 1e9 / peaks["bf16_tflops"],
-                                      "dense_equiv_TFLOP/s": fl_dense_eq / t_pru / 1e9}
-    rows["restore_scatter_48to64"] = {"ms": t_res, "bytes": res_bytes, "GB/s": res_bytes / t_res / 1e6,
-                                      "frac_hbm": res_bytes / t_res / 1e6 / peaks["hbm_gbs"]}
-    t_chain = t_piv + t_pru + t_res
-    rows["pruned_step_64x64_total"] = {"ms": t_chain, "dense_equiv_TFLOP/s": fl_dense_eq / t_chain / 1e9}
-    del x, q, k, v, prev, wsb, idx, oc, out
-    # --- block-sparse final step of the 2K schedule
+    flush = L2Flush(dev)
+    calls = step.calls()
+    t = time_graph(calls[1], iters, flush)
+    rows["pivot_select_64x64_alone"] = {"ms": t, "GB/s": step.bytes_pivot / t / 1e6,
+                                        "frac_hbm": step.bytes_pivot / t / 1e6 / peaks["hbm_gbs"],
+                                        "timing": "CUDA graph replay after an L2 flush"}
+    t = time_graph(calls[3], iters, flush)
+    rows["restore_scatter_48to64_alone"] = {"ms": t, "GB/s": step.bytes_restore / t / 1e6,
+                                            "frac_hbm": step.bytes_restore / t / 1e6 / peaks["hbm_gbs"],
+                                            "timing": "CUDA graph replay after an L2 flush"}
+    # block-sparse attention on the 2K schedule (its own workload)
     w = WORKLOADS["blocksparse_2k"]
-    step = w.steps[-1]
+    st = w.steps[-1]
     B, H, D = w.batch, w.heads, w.head_dim
     p = V.problem(B, H, D, w.sides)
-    try:
-        row_ptr, entries, sink_len = V.var_block_mask_build(p, step, w.qblock_side, w.radius, w.sink_max_side)
-        inp = make_inputs(w)
-        q, k, v = inp.q[step].to(dev), inp.k.to(dev), inp.v.to(dev)
-        o = torch.empty_like(q)
-        rp = torch.as_tensor(row_ptr, device=dev)
-        en = torch.as_tensor(entries, device=dev)
-        m = V.block_mask_struct(w.qblock_side, rp, en, sink_len)
+    rp, en, sink = V.var_block_mask_build(p, st, w.qblock_side, w.radius, w.sink_max_side)
+    inp = make_inputs(w)
+    q, k, v = inp.q[st].to(dev), inp.k.to(dev), inp.v.to(dev)
+    del inp
+    o = torch.empty_like(q)
+    m = V.block_mask_struct(w.qblock_side, torch.as_tensor(rp, device=dev), torch.as_tensor(en, device=dev), sink)
+    stream = torch.cuda.current_stream(dev)
 
-        def bs():
-            V.var_attn_blocksparse(p, step, q, k, v, m, o, stream=stream)
+    def bs():
+        V.var_attn_blocksparse(p, st, q, k, v, m, o, stream=stream)
 
-        for _ in range(3):
-            bs()
-        t_bs = time_loop(bs, steps, stream)
-        N = q.shape[2]
-        L = cache_len(w.sides, step)
-        # algorithmic FLOPs: 4*D per kept (query, key) pair, from the CSR
-        kept_pairs = 0
-        sides = w.sides
-        for qb in range(len(row_ptr) - 1):
-            nk = sink_len
-            for e in entries[row_ptr[qb]:row_ptr[qb + 1]]:
-                sc, u, vv = e >> 24, (e >> 12) & 0xFFF, e & 0xFFF
-                s = sides[sc]
-                nk += (min(s, u * 8 + 8) - u * 8) * (min(s, vv * 8 + 8) - vv * 8)
-            kept_pairs += nk * 64
-        fl = 4.0 * B * H * kept_pairs * D
-        rows["attn_blocksparse_2k"] = {"ms": t_bs, "TFLOP/s": fl / t_bs / 1e9,
-                                       "frac_tensor": fl / t_bs / 1e9 / peaks["bf16_tflops"],
-                                       "dense_equiv_TFLOP/s": 4.0 * B * H * N * L * D / t_bs / 1e9,
-                                       "density": kept_pairs / (N * L)}
-    except V.VarError as e:
-        rows["attn_blocksparse_2k"] = {"unavailable": str(e)}
+    for _ in range(3):
+        bs()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(5, iters)
+    e0.record(stream)
+    for _ in range(n):
+        bs()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / n
+    N, L = q.shape[2], cache_len(w.sides, st)
+    pairs = mask_kept_pairs(w.sides, rp, en, sink, w.qblock_side)
+    fl = 4.0 * B * H * pairs * D
+    rows["attn_blocksparse_2k"] = {"ms": t, "TFLOP/s": fl / t / 1e9, "frac_tensor": fl / t / 1e9 / peaks["bf16_tflops"],
+                                   "dense_equiv_TFLOP/s": flops_attn(B, H, N, L, D) / t / 1e9,
+                                   "density": pairs / (N * L)}
+    del q, k, v, o
+    # the whole 256px schedule, dense (launch-bound)
+    w = WORKLOADS["dense_256px"]
+    inp = make_inputs(w)
+    B, H, D = w.batch, w.heads, w.head_dim
+    p = V.problem(B, H, D, w.sides)
+    k, v = inp.k.to(dev), inp.v.to(dev)
+    qs = {s: inp.q[s].to(dev) for s in w.steps}
+    os_ = {s: torch.empty_like(qs[s]) for s in w.steps}
+
+    def sched():
+        for s in w.steps:
+            V.var_attn_dense(p, s, qs[s], k, v, os_[s])
+
+    t = time_graph(sched, iters, flush)
+    fl = sum(flops_attn(B, H, w.sides[s] ** 2, cache_len(w.sides, s), D) for s in w.steps)
+    rows["schedule_256px_dense_10_steps"] = {"ms": t, "TFLOP/s": fl / t / 1e9, "launches": len(w.steps),
+                                             "timing": "CUDA graph replay after an L2 flush"}
     return rows
 
 
@@ -339,88 +442,127 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     import visual_autoregressive_next_var_b300 as V
 
-    w = WORKLOADS[args.workload]
-    step = w.steps[-1]
-    inp = make_inputs(w, steps=(step,))
-    q_h = inp.q[step]
-    B, H, N, D = q_h.shape
-    L = cache_len(w.sides, step)
-    p = V.problem(B, H, D, w.sides, kv_capacity=inp.k.shape[2])
-    q, k, v = q_h.to(dev), inp.k.to(dev), inp.v.to(dev)
-    o = torch.empty_like(q)
+    inp = make_inputs(WORKLOADS[STEP_WORKLOAD], steps=(FINAL - 1, FINAL))
+    step = Step(V, dev, inp)
     stream = torch.cuda.current_stream(dev)
-    flops = 4.0 * B * H * N * L * D
-    in_bytes = (q.numel() + k.numel() + v.numel()) * 2
-
-    def step_fn():
-        V.var_attn_dense(p, step, q, k, v, o, stream=stream)
+    flops_equiv = 3.0 * step.flops_dense
+    flops_exec = step.flops_dense + step.flops_pruned + step.flops_sparse
 
     for _ in range(args.warmup):
-        step_fn()
+        step.run(stream)
     torch.cuda.synchronize()
     barrier(ws)
     with ClockSampler(local, enabled=not args.no_clocks) as clk:
         if not args.no_clocks:
-            # keep the GPU busy (untimed) until the sampler is producing, then time
-            t0 = time.perf_counter()
+            t0 = time.perf_counter()            # keep the GPU busy (untimed) until the sampler runs
             while time.perf_counter() - t0 < 0.4:
-                step_fn()
+                step.run(stream)
                 torch.cuda.synchronize()
             barrier(ws)
-        ms = time_loop(step_fn, args.steps, stream)
+        ms, per_row = time_step(step, args.steps, stream)
     ms_max = reduce_max(ms, ws, dev)
     st = V.var_device_status()
     if st != 0:
         raise RuntimeError(f"device status {st} ({V.var_status_string(st)})")
     peaks = load_peaks()
-    achieved = flops / ms / 1e9                      # TFLOP/s of this rank's kernel
-    value = ws * flops / ms_max / 1e9
+    value = ws * flops_equiv / ms_max / 1e9
+
+    # per-row figures inside the timed region
+    row_flops = {"attn_dense": step.flops_dense, "attn_pruned": step.flops_pruned,
+                 "attn_blocksparse": step.flops_sparse}
+    row_bytes = {"pivot_select": step.bytes_pivot, "restore_scatter": step.bytes_restore}
+    rows = {}
+    for name, t in zip(ROW_NAMES, per_row):
+        r = {"ms": t}
+        if name in row_flops:
+            r["TFLOP/s"] = row_flops[name] / t / 1e9
+            r["frac_tensor"] = r["TFLOP/s"] / peaks["bf16_tflops"]
+            r["dense_equiv_TFLOP/s"] = step.flops_dense / t / 1e9
+        else:
+            r["GB/s"] = row_bytes[name] / t / 1e6
+            r["frac_hbm"] = r["GB/s"] / peaks["hbm_gbs"]
+        rows[name] = r
+    rows["attn_blocksparse"]["density"] = step.sparse_pairs / (step.N * step.L)
+    rows["block_mask_build_host_once"] = {"ms": step.mask_build_ms}
+    dom = max(range(len(ROW_NAMES)), key=lambda i: per_row[i])
+    dom_name = ROW_NAMES[dom]
+    kernel_names = {"attn_dense": "attn_kernel<128, dense>", "attn_pruned": "attn_kernel<128, gather>",
+                    "attn_blocksparse": "attn_kernel<128, sparse>", "pivot_select": "pivot kernels",
+                    "restore_scatter": "restore_scatter_kernel<128>"}
+    if dom_name in row_flops:
+        achieved = row_flops[dom_name] / per_row[dom] / 1e9
+        roof = {"kernel": kernel_names[dom_name], "bound": "tensor", "achieved": achieved,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "peak_source": f"{peaks['source']} dense bf16 burst (cuBLAS)",
+                "traffic": ncu_traffic(f"{kernel_names[dom_name]}:final_step_1024px"),
+                "algorithmic_flops_per_launch": row_flops[dom_name],
+                "launch_ms": per_row[dom]}
+    else:
+        achieved = row_bytes[dom_name] / per_row[dom] / 1e6
+        roof = {"kernel": kernel_names[dom_name], "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "peak_source": f"{peaks['source']} copy",
+                "traffic": ncu_traffic(f"{kernel_names[dom_name]}:final_step_1024px"),
+                "algorithmic_bytes_per_launch": row_bytes[dom_name], "launch_ms": per_row[dom]}
 
     # end to end through the public API with host buffers
-    qp = q_h.pin_memory()
-    kp = inp.k.pin_memory()
-    vp = inp.v.pin_memory()
-    op = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    host = {"q": inp.q[FINAL].pin_memory(), "k": inp.k.pin_memory(), "v": inp.v.pin_memory(),
+            "x": inp.x[FINAL].pin_memory(), "prev": step.prev.cpu().pin_memory()}
+    outs = {"o_dense": torch.empty(step.o_dense.shape, dtype=torch.bfloat16).pin_memory(),
+            "idx": torch.empty(step.idx.shape, dtype=torch.int32).pin_memory(),
+            "o_pruned": torch.empty(step.o_pruned.shape, dtype=torch.bfloat16).pin_memory(),
+            "o_sparse": torch.empty(step.o_sparse.shape, dtype=torch.bfloat16).pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs.values())
 
     def e2e_fn():
-        q.copy_(qp, non_blocking=True)
-        k.copy_(kp, non_blocking=True)
-        v.copy_(vp, non_blocking=True)
-        V.var_attn_dense(p, step, q, k, v, o, stream=stream)
-        op.copy_(o, non_blocking=True)
+        step.q.copy_(host["q"], non_blocking=True)
+        step.k.copy_(host["k"], non_blocking=True)
+        step.v.copy_(host["v"], non_blocking=True)
+        step.x.copy_(host["x"], non_blocking=True)
+        step.prev.copy_(host["prev"], non_blocking=True)
+        step.run(stream)
+        outs["o_dense"].copy_(step.o_dense, non_blocking=True)
+        outs["idx"].copy_(step.idx, non_blocking=True)
+        outs["o_pruned"].copy_(step.o_pruned, non_blocking=True)
+        outs["o_sparse"].copy_(step.o_sparse, non_blocking=True)
 
     for _ in range(2):
         e2e_fn()
     e2e_steps = max(3, min(args.steps, 10))
-    ms_e2e = reduce_max(time_loop(e2e_fn, e2e_steps, stream), ws, dev)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = reduce_max(e0.elapsed_time(e1) / e2e_steps, ws, dev)
 
+    cfg = step_config(inp)
+    cfg["l2"] = "inputs larger than L2 (Q/K/V 206 MB + X 34 MB per step)"
+    cfg["per_gpu"] = "each rank runs the whole workload"
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "batch": B, "heads": H, "head_dim": D, "queries": N,
-                   "keys": L, "kv_tokens_total": inp.k.shape[2],
-                   "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB of Q/K/V)",
-                   "per_gpu": "each rank runs the whole workload"},
-        "roofline": {"kernel": "attn_kernel<128, dense>", "bound": "tensor", "achieved": achieved,
-                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": achieved / peaks["bf16_tflops"],
-                     "peak_source": f"{peaks['source']} dense bf16 burst (cuBLAS)",
-                     "traffic": ncu_traffic("attn_kernel<128, dense>:" + w.name, 1.0),
-                     "algorithmic_flops_per_launch": flops},
-        "e2e": {"value": ws * flops / ms_e2e / 1e9, "unit": "TFLOP/s", "ms_per_step": ms_e2e,
-                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": o.numel() * 2},
-        "gpu_launches": args.steps,
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+        "value_note": "dense-equivalent: 3 x the final-scale dense attention FLOPs per step "
+                      f"({flops_equiv / 1e9:.1f} GFLOP); executed algorithmic FLOPs "
+                      f"{flops_exec / 1e9:.1f} GFLOP -> {ws * flops_exec / ms_max / 1e9:.1f} TFLOP/s",
+        "roofline": roof,
+        "e2e": {"value": ws * flops_equiv / ms_e2e / 1e9, "unit": "TFLOP/s", "ms_per_step": ms_e2e,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * LAUNCHES_PER_STEP,
         "clocks": clk.summary(),
+        "rows": rows,
     }
     if not args.no_rows:
-        line["rows"] = bench_rows(V, dev, stream, max(5, args.steps // 2))
+        line["rows"].update(extra_rows(V, dev, step, max(5, min(args.steps, 20)), peaks))
     if rank == 0 and ws == 1 and not args.no_cpu:
-        n_rows = oracle_calibrate(w, inp, step, args.cpu_seconds)
-        tf, dt, thr = oracle_run(w, inp, step, n_rows)
+        tf, dt, n_rows, thr = oracle_sample(inp, args.cpu_seconds)
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
-                                "sample": f"{n_rows} random query rows of the final step "
-                                          f"(of {B * H * N}), {dt:.1f} s; throughput per FLOP"}
+                                "sample": f"{n_rows} random query rows of the final step's dense attention "
+                                          f"(of {step.q.shape[0] * step.q.shape[1] * step.N}), {dt:.1f} s; "
+                                          "throughput per FLOP"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -432,11 +574,10 @@ def run_gpu(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("varattn", "reference"), default="varattn")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=HEADLINE)
-    ap.add_argument("--no-rows", action="store_true", help="skip the per-kernel rows")
+    ap.add_argument("--no-rows", action="store_true", help="skip the separate per-kernel measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-clocks", action="store_true", help="no nvidia-smi sampling (profiler runs)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
