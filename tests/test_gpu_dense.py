@@ -88,6 +88,26 @@ def test_dense_1024px_sampled_rows_and_determinism():
     check_device_status()
 
 
+def test_dense_split_tail_ctas_every_row():
+    """160 pair slots on 148 SMs: the last 12 slots run as 24 one-tile CTAs whose
+    two softmax groups take alternate key tiles and merge at the end; check
+    every row of the (b, h) those CTAs cover, and of the first (b, h)."""
+    sides, D, B, H = (1, 2, 4, 8, 16, 32), 128, 2, 20
+    step = len(sides) - 1
+    L, N = cache_len(sides, step), sides[step] ** 2
+    q = randn_bf16((B, H, N, D), 11)
+    k = randn_bf16((B, H, L, D), 12)
+    v = randn_bf16((B, H, L, D), 13)
+    p = V.problem(B, H, D, sides)
+    o = run_dense(p, step, q, k, v)
+    bhs = [0, B * H - 3, B * H - 2, B * H - 1]
+    rows = np.concatenate([np.arange(bh * N, (bh + 1) * N) for bh in bhs])
+    ref = oracle.attention(q, k, v, L, rows=rows)
+    got = o.reshape(-1, D)[torch.as_tensor(rows, device=DEV)]
+    assert_close(got, ref, "dense split tail")
+    check_device_status()
+
+
 def test_dense_invariants_on_gpu():
     # identical value rows -> that row; all-equal keys -> mean of values
     B, H, D, sides = 1, 2, 128, (1, 2, 4, 8, 16)

@@ -1,8 +1,82 @@
 // Dense and pruned (gathered-query) cross-scale attention: host launchers of
 // the shared kernel in attn_kernel.cuh.
+#include <map>
+#include <mutex>
+#include <queue>
+#include <tuple>
+#include <vector>
+
 #include "attn_kernel.cuh"
 
 namespace varattn {
+
+// ---------------------------------------------------------------------------- CTA plan
+
+// A pair CTA runs two 128-row query tiles against every key tile; a split CTA
+// runs one tile with its key tiles shared out between the two softmax groups
+// (about half the pair's time).  Plan A: all pair slots as pair CTAs (plus the
+// odd last tiles as split CTAs).  Plan B: pair CTAs for whole waves only, the
+// rest as split CTAs, which shortens a partial last wave of pairs.  The plan
+// with the smaller greedy-dispatch makespan is used; plans are cached per shape.
+struct TilePlan {
+    int n_pair_ctas, n_conv_slots, grid;
+};
+
+static double dispatch_makespan(int pairs, int singles, int n_sms)
+{
+    constexpr double kSplitCost = 0.6;   // split CTA time relative to a pair CTA
+    std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+    for (int i = 0; i < n_sms; ++i) free_at.push(0.0);
+    double end = 0.0;
+    for (int i = 0; i < pairs + singles; ++i) {
+        const double t = free_at.top() + (i < pairs ? 1.0 : kSplitCost);
+        free_at.pop();
+        free_at.push(t);
+        end = t > end ? t : end;
+    }
+    return end;
+}
+
+static int sm_count()
+{
+    static std::mutex mu;
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+static TilePlan plan_tiles(int bh, int tiles_per_bh)
+{
+    const int n_sms = sm_count();
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int>, TilePlan> cache;
+    const auto key = std::make_tuple(bh, tiles_per_bh, n_sms);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    const int slots = bh * (tiles_per_bh / 2);
+    const int odd = (tiles_per_bh & 1) ? bh : 0;
+    TilePlan a{slots, 0, slots + odd};
+    const int keep = n_sms * (slots / n_sms);
+    TilePlan b{keep, slots - keep, keep + 2 * (slots - keep) + odd};
+    TilePlan best = a;
+    if (b.n_conv_slots > 0 && slots + odd <= 1 << 16 &&
+        dispatch_makespan(b.n_pair_ctas, b.grid - b.n_pair_ctas, n_sms) <
+            dispatch_makespan(a.n_pair_ctas, a.grid - a.n_pair_ctas, n_sms) - 1e-9)
+        best = b;
+    std::lock_guard<std::mutex> lk(mu);
+    cache[key] = best;
+    return best;
+}
 
 // ---------------------------------------------------------------------------- host
 
@@ -45,14 +119,18 @@ static int launch_attn(const StepGeom& g, const void* q, const void* k, const vo
     a.n_q = g.N;
     a.L = g.L;
     a.heads = g.H;
-    a.pairs_per_bh = (n_rows + 255) / 256;
+    a.tiles_per_bh = (n_rows + 127) / 128;
+    a.slots_per_bh = a.tiles_per_bh / 2;
+    const TilePlan plan = plan_tiles(static_cast<int>(BH), a.tiles_per_bh);
+    a.n_pair_ctas = plan.n_pair_ctas;
+    a.n_conv_slots = plan.n_conv_slots;
     a.n_kv = (g.L + 127) / 128;
     a.scale_log2 = g.scale * 1.4426950408889634f;
     a.q = static_cast<const __nv_bfloat16*>(q);
     a.idx = idx;
     a.o = static_cast<__nv_bfloat16*>(o);
     a.status = status;
-    const dim3 grid(static_cast<unsigned>(BH * a.pairs_per_bh));
+    const dim3 grid(static_cast<unsigned>(plan.grid));
     kern<<<grid, 384, Lay::SMEM_BYTES, st>>>(maps, a);
     return cuda_status(cudaGetLastError());
 }

@@ -96,7 +96,16 @@ struct AttnArgs {
     int32_t n_q;            // rows of the Q tensor per (b,h)
     int32_t L;              // visible cached keys
     int32_t heads;
-    int32_t pairs_per_bh;   // ceil(n_rows / 256)             (dense, gather)
+    // CTA schedule (dense, gather).  A (b,h) has tiles_per_bh 128-row query
+    // tiles, grouped into pair slots (tiles 2k, 2k+1).  CTAs [0, n_pair_ctas)
+    // take pair slots in order; the other CTAs take one tile each ("split"
+    // CTAs: the two softmax groups share that tile and take alternate key
+    // tiles): first both tiles of the remaining pair slots, then the last tile
+    // of each (b,h) when tiles_per_bh is odd.
+    int32_t tiles_per_bh;
+    int32_t slots_per_bh;   // tiles_per_bh / 2
+    int32_t n_pair_ctas;
+    int32_t n_conv_slots;   // pair slots taken by two split CTAs
     int32_t n_kv;           // ceil(L / 128)                   (dense, gather)
     float scale_log2;       // softmax scale * log2(e)
     const __nv_bfloat16* q; // gather source (pruned)
@@ -295,6 +304,7 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
     const int2* U = reinterpret_cast<const int2*>(smem + Lay::OFF_U);
 
     int bh, row0 = 0, by0 = 0, bx0 = 0;
+    bool split = false;        // one query tile; group g takes key tiles j = g (mod 2)
     if constexpr (SPARSE) {
         const int nsq2 = args.nsq * args.nsq;
         bh = blockIdx.x / nsq2;
@@ -302,8 +312,23 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
         by0 = 2 * (sq / args.nsq);
         bx0 = 2 * (sq % args.nsq);
     } else {
-        bh = blockIdx.x / args.pairs_per_bh;
-        row0 = (blockIdx.x % args.pairs_per_bh) * 256;
+        const int c = static_cast<int>(blockIdx.x);
+        if (c < args.n_pair_ctas) {
+            bh = c / args.slots_per_bh;
+            row0 = (c - bh * args.slots_per_bh) * 256;
+        } else {
+            split = true;
+            const int sgl = c - args.n_pair_ctas;
+            const int n_conv = args.n_conv_slots;            // pair slots taken as two split CTAs
+            if (sgl < 2 * n_conv) {
+                const int slot = args.n_pair_ctas + sgl / 2;
+                bh = slot / args.slots_per_bh;
+                row0 = (slot - bh * args.slots_per_bh) * 256 + (sgl & 1) * 128;
+            } else {
+                bh = sgl - 2 * n_conv;
+                row0 = (args.tiles_per_bh - 1) * 128;
+            }
+        }
     }
 
     if (threadIdx.x == 0) {
@@ -364,7 +389,7 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
                                         bar(Lay::B_QF + t));
                 }
             } else if constexpr (!GATHER) {
-                for (int t = 0; t < 2; ++t) {
+                for (int t = 0; t < (split ? 1 : 2); ++t) {
                     mbar_arrive_expect_tx(bar(Lay::B_QF + t), Lay::TILE_BYTES);
                     for (int hh = 0; hh < Lay::HALVES; ++hh)
                         tma_load_3d(sbase + Lay::OFF_Q + t * Lay::TILE_BYTES + hh * Lay::HALF_BYTES,
@@ -424,15 +449,15 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
             for (int j = (v_issued > NS ? v_issued - NS : 0); j < v_issued; ++j)
                 mbar_wait(bar(Lay::B_VF + j % NS), (j / NS) & 1, nullptr);
             if (!GATHER)
-                for (int t = 0; t < 2; ++t) mbar_wait(bar(Lay::B_QF + t), 0, nullptr);
+                for (int t = 0; t < (split ? 1 : 2); ++t) mbar_wait(bar(Lay::B_QF + t), 0, nullptr);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ UMMA issuer
         if (lane == 0) {
             constexpr uint32_t IDESC_QK = idesc_bf16(128, 128, false, false);
             constexpr uint32_t IDESC_PV = idesc_bf16(128, D, false, true);
-            auto qk = [&](int t, int s) {
-                const uint32_t qa = sbase + Lay::OFF_Q + t * Lay::TILE_BYTES;
+            auto qk = [&](int t, int s, int qt) {   // S_t = Q_qt K_s^T
+                const uint32_t qa = sbase + Lay::OFF_Q + qt * Lay::TILE_BYTES;
                 const uint32_t kb = sbase + Lay::OFF_K + s * Lay::TILE_BYTES;
                 const uint32_t dst = tmem + (t ? Lay::COL_S1 : Lay::COL_S0);
 #pragma unroll
@@ -452,43 +477,73 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
                             IDESC_PV, (acc || kk > 0) ? 1u : 0u);
             };
             bool ok = mbar_wait(bar(Lay::B_QF + 0), 0, abort_flag) &&
-                      mbar_wait(bar(Lay::B_QF + 1), 0, abort_flag);
-            if (ok && n_kv > 0) {
-                ok = mbar_wait(bar(Lay::B_KF + 0), 0, abort_flag);
-                if (ok) {
+                      (split || mbar_wait(bar(Lay::B_QF + 1), 0, abort_flag));
+            if (split) {
+                // one query tile; group g takes key tiles j = g, g + 2, ...: its
+                // S_g = Q_0 K_j^T, O_g += P_g V_j; each K / V tile is used once
+                for (int g0 = 0; g0 < 2 && ok && g0 < n_kv; ++g0) {
+                    if (!(ok = mbar_wait(bar(Lay::B_KF + g0 % NS), (g0 / NS) & 1, abort_flag))) break;
                     tc_fence_after();
-                    qk(0, 0);
-                    umma_commit(bar(Lay::B_SF + 0));
-                    qk(1, 0);
-                    umma_commit(bar(Lay::B_SF + 1));
-                    umma_commit(bar(Lay::B_KE + 0));
+                    qk(g0, g0 % NS, 0);
+                    umma_commit(bar(Lay::B_SF + g0));
+                    umma_commit(bar(Lay::B_KE + g0 % NS));
                 }
-            }
-            for (int j = 0; ok && j < n_kv; ++j) {
-                const int s = j % NS;
-                const uint32_t ph = (j / NS) & 1;
-                const bool more = j + 1 < n_kv;
-                const int s1 = (j + 1) % NS;
-                const uint32_t ph1 = ((j + 1) / NS) & 1;
-                ok = mbar_wait(bar(Lay::B_VF + s), ph, abort_flag) &&
-                     mbar_wait(bar(Lay::B_PF + 0), j & 1, abort_flag);
-                if (!ok) break;
-                tc_fence_after();
-                pv(0, s, j > 0);
-                if (more) {
-                    if (!(ok = mbar_wait(bar(Lay::B_KF + s1), ph1, abort_flag))) break;
+                for (int j = 0; ok && j < n_kv; ++j) {
+                    const int g1 = j & 1, jj = j >> 1;
+                    const int s = j % NS;
+                    if (!(ok = mbar_wait(bar(Lay::B_VF + s), (j / NS) & 1, abort_flag) &&
+                               mbar_wait(bar(Lay::B_PF + g1), jj & 1, abort_flag)))
+                        break;
                     tc_fence_after();
-                    qk(0, s1);
-                    umma_commit(bar(Lay::B_SF + 0));
+                    pv(g1, s, jj > 0);
+                    umma_commit(bar(Lay::B_VE + s));
+                    const int jn = j + 2;
+                    if (jn < n_kv) {
+                        if (!(ok = mbar_wait(bar(Lay::B_KF + jn % NS), (jn / NS) & 1, abort_flag))) break;
+                        tc_fence_after();
+                        qk(g1, jn % NS, 0);
+                        umma_commit(bar(Lay::B_SF + g1));
+                        umma_commit(bar(Lay::B_KE + jn % NS));
+                    }
                 }
-                if (!(ok = mbar_wait(bar(Lay::B_PF + 1), j & 1, abort_flag))) break;
-                tc_fence_after();
-                pv(1, s, j > 0);
-                umma_commit(bar(Lay::B_VE + s));
-                if (more) {
-                    qk(1, s1);
-                    umma_commit(bar(Lay::B_SF + 1));
-                    umma_commit(bar(Lay::B_KE + s1));
+            } else {
+                if (ok && n_kv > 0) {
+                    ok = mbar_wait(bar(Lay::B_KF + 0), 0, abort_flag);
+                    if (ok) {
+                        tc_fence_after();
+                        qk(0, 0, 0);
+                        umma_commit(bar(Lay::B_SF + 0));
+                        qk(1, 0, 1);
+                        umma_commit(bar(Lay::B_SF + 1));
+                        umma_commit(bar(Lay::B_KE + 0));
+                    }
+                }
+                for (int j = 0; ok && j < n_kv; ++j) {
+                    const int s = j % NS;
+                    const uint32_t ph = (j / NS) & 1;
+                    const bool more = j + 1 < n_kv;
+                    const int s1 = (j + 1) % NS;
+                    const uint32_t ph1 = ((j + 1) / NS) & 1;
+                    ok = mbar_wait(bar(Lay::B_VF + s), ph, abort_flag) &&
+                         mbar_wait(bar(Lay::B_PF + 0), j & 1, abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    pv(0, s, j > 0);
+                    if (more) {
+                        if (!(ok = mbar_wait(bar(Lay::B_KF + s1), ph1, abort_flag))) break;
+                        tc_fence_after();
+                        qk(0, s1, 0);
+                        umma_commit(bar(Lay::B_SF + 0));
+                    }
+                    if (!(ok = mbar_wait(bar(Lay::B_PF + 1), j & 1, abort_flag))) break;
+                    tc_fence_after();
+                    pv(1, s, j > 0);
+                    umma_commit(bar(Lay::B_VE + s));
+                    if (more) {
+                        qk(1, s1, 1);
+                        umma_commit(bar(Lay::B_SF + 1));
+                        umma_commit(bar(Lay::B_KE + s1));
+                    }
                 }
             }
             if (!ok) record_fault(abort_flag, args.status, VAR_ERR_TIMEOUT);
@@ -507,7 +562,7 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
         const int qrow = row0 + g * 128 + r;
         const int q4 = 2 * g + (r >> 6);     // block of the square (block-sparse); warp-uniform
 
-        if constexpr (GATHER) {
+        if (GATHER && !(split && g == 1)) {
             // This thread's query row, gathered by index, into the swizzled tile.
             const int b = bh / args.heads;
             uint8_t* qs = smem + Lay::OFF_Q + g * Lay::TILE_BYTES;
@@ -537,8 +592,11 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
         float m_run = -INFINITY;
         float l_run = 0.f;
         bool ok = true;
-        for (int j = 0; j < n_kv; ++j) {
-            if (!mbar_wait(bar(Lay::B_SF + g), j & 1, abort_flag)) {
+        // a split CTA's group g takes key tiles j = g, g + 2, ...
+        const int n_local = split ? (n_kv + 1 - g) / 2 : n_kv;
+        for (int jj = 0; jj < n_local; ++jj) {
+            const int j = split ? 2 * jj + g : jj;
+            if (!mbar_wait(bar(Lay::B_SF + g), jj & 1, abort_flag)) {
                 ok = false;
                 break;
             }
@@ -628,7 +686,7 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
             }
             // O_t *= alpha where the running maximum moved (the previous PV has
             // completed: its commit preceded this tile's S commit)
-            if (__any_sync(0xffffffffu, need && j > 0)) {
+            if (__any_sync(0xffffffffu, need && jj > 0)) {
 #pragma unroll
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t o[32];
@@ -644,9 +702,26 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
             mbar_arrive(bar(Lay::B_PF + g));
         }
         if (ok) ok = mbar_wait(bar(Lay::B_OF), 0, abort_flag);
+        // split CTA: group 1 hands its row's (m, l) to group 0, which merges
+        // O_0 and O_1 (both in its tensor-memory lanes) into the output
+        float2* comb = reinterpret_cast<float2*>(smem + Lay::OFF_K);   // the K ring is idle now
+        float a0 = 1.f, a1 = 0.f;
+        if (split) {
+            if (g == 1) {
+                if (ok) comb[r] = make_float2(m_run, l_run);
+                named_bar_arrive(1, 256);
+            } else {
+                named_bar_sync(1, 256);
+                const float2 ml = comb[r];
+                const float mm = fmaxf(m_run, ml.x);
+                a0 = l_run > 0.f ? ex2_approx(m_run - mm) : 0.f;
+                a1 = ml.y > 0.f ? ex2_approx(ml.x - mm) : 0.f;
+                l_run = l_run * a0 + ml.y * a1;
+            }
+        }
         if (!ok) {
             record_fault(abort_flag, args.status, VAR_ERR_TIMEOUT);
-        } else {
+        } else if (!split || g == 0) {
             tc_fence_after();
             // destination row of this thread, or none
             __nv_bfloat16* dst = nullptr;
@@ -661,10 +736,20 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
             }
             const bool any = l_run > 0.f;            // a row that kept no key is written as zeros
             const float inv = any ? 1.0f / l_run : 0.f;
+            const uint32_t tO1 = tmem + lane_base + Lay::COL_O1;
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t o[32];
                 tmem_ld32(tO + c0, o);
+                if (split) {
+                    uint32_t o1[32];
+                    tmem_ld32(tO1 + c0, o1);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        o[c] = __float_as_uint(__uint_as_float(o[c]) * a0 +
+                                               (a1 != 0.f ? __uint_as_float(o1[c]) * a1 : 0.f));
+                }
                 tmem_wait_ld();
                 if (dst) {
                     uint32_t w[16];
