@@ -379,6 +379,23 @@ def extra_rows(V, dev, step: Step, iters: int, peaks):
     rows["restore_scatter_48to64_alone"] = {"ms": t, "GB/s": step.bytes_restore / t / 1e6,
                                             "frac_hbm": step.bytes_restore / t / 1e6 / peaks["hbm_gbs"],
                                             "timing": "CUDA graph replay after an L2 flush"}
+    # the pruned step with the outputs written in place (no compact buffer)
+    def fused():
+        step.V.var_attn_pruned_scatter(step.p, FINAL, step.q, step.k, step.v, step.idx, step.K, step.o_pruned)
+        step.V.var_restore_fill(step.p, FINAL, step.prev, step.idx, step.K, step.o_pruned)
+
+    t = time_graph(fused, iters, flush)
+    t_chain = time_graph(lambda: (calls[2](), calls[3]()), iters, flush)
+    rows["pruned_attn_and_restore_fused"] = {"ms": t, "unfused_ms": t_chain,
+                                             "dense_equiv_TFLOP/s": step.flops_dense / t / 1e9,
+                                             "timing": "CUDA graph replay after an L2 flush"}
+    # Branch Halving: the conditional half only, its rows repeated
+    t = time_graph(lambda: step.V.var_attn_dense_halved(step.p, FINAL, step.q, step.k, step.v, step.o_dense),
+                   iters, flush)
+    rows["attn_dense_branch_halved"] = {"ms": t, "TFLOP/s": step.flops_dense / 2 / t / 1e9,
+                                        "frac_tensor": step.flops_dense / 2 / t / 1e9 / peaks["bf16_tflops"],
+                                        "dense_equiv_TFLOP/s": step.flops_dense / t / 1e9,
+                                        "timing": "CUDA graph replay after an L2 flush"}
     # block-sparse attention on the 2K schedule (its own workload)
     w = WORKLOADS["blocksparse_2k"]
     st = w.steps[-1]

@@ -147,6 +147,47 @@ VAR_API int var_attn_pruned(const var_problem* p, int32_t step, const void* q, c
                     void* stream);
 
 /*
+ * Pruned attention with the outputs written in place ("ARVAR" Key Design 3,
+ * Eq. (8)-(9): the sparse outputs are scattered back to their retained
+ * positions): as var_attn_pruned, but the row for query idx[b, j] goes to
+ * out[b, h, idx[b, j], :] of the full-grid output instead of a compact buffer.
+ * Together with var_restore_fill, which writes every other row, this computes
+ * the same out as var_attn_pruned followed by var_restore_scatter without the
+ * compact buffer's write and read.  Rows not in idx are not touched.
+ * q: [B][H][N][D]; idx: [B][keep_k] int32 device, distinct, each in [0, N);
+ * out: [B][H][N][D].  keep_k = 0 is a no-op.
+ * Errors: as var_attn_pruned.
+ */
+VAR_API int var_attn_pruned_scatter(const var_problem* p, int32_t step, const void* q, const void* k,
+                                    const void* v, const int32_t* idx, int32_t keep_k, void* out,
+                                    void* stream);
+
+/*
+ * The reconstruction's upsampled part alone ("ARVAR" Eq. (8)-(9)): writes
+ * Up(prev; s, s) to every row of out whose token is NOT in idx[b, :] and leaves
+ * the rows in idx untouched (var_attn_pruned_scatter writes those).  The two
+ * calls write disjoint rows, so they may run in either order or concurrently.
+ * prev: [B][H][s'^2][D]; idx: [B][keep_k] strictly ascending, in [0, s^2);
+ * out: [B][H][s^2][D].  step >= 1.
+ * Errors: as var_restore_scatter.
+ */
+VAR_API int var_restore_fill(const var_problem* p, int32_t step, const void* prev, const int32_t* idx,
+                             int32_t keep_k, void* out, void* stream);
+
+/*
+ * Dense attention under Branch Halving ("ARVAR" Key Design 1: at a selected
+ * step only the conditional branch goes through the block and its output is
+ * repeated to restore the two-branch interface).  The batch is the two
+ * classifier-free-guidance branches concatenated, the conditional half first:
+ * batch elements [0, B/2) are computed as in var_attn_dense and each output
+ * row is written to both o[b] and o[b + B/2].  The second half of q, k and v
+ * is not read.  B must be even.
+ * Errors: as var_attn_dense, plus VAR_ERR_INVALID_ARG for an odd batch.
+ */
+VAR_API int var_attn_dense_halved(const var_problem* p, int32_t step, const void* q, const void* k,
+                                  const void* v, void* o, void* stream);
+
+/*
  * Structural reconstruction ("ARVAR" Key Design 3, Eq. (8)-(9)):
  *   out = Scatter(Up(prev; s, s), idx, o_compact)
  * Up is bilinear interpolation of the previous step's s' x s' output grid

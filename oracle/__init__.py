@@ -106,6 +106,19 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, L: int,
     return out
 
 
+def branch_halved_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, L: int,
+                            scale: Optional[float] = None) -> np.ndarray:
+    """Branch Halving ("ARVAR" Key Design 1): only the conditional branch -- the
+    first half of the batch, the classifier-free-guidance pair concatenated along
+    the batch -- is computed; its output is repeated into the second half.
+    Returns [B, H, N, D] fp64."""
+    B = q.shape[0]
+    assert B % 2 == 0
+    h = B // 2
+    cond = attention(q[:h].contiguous(), k[:h].contiguous(), v[:h].contiguous(), L, scale=scale)
+    return np.concatenate([cond, cond], axis=0)
+
+
 def block_mask_rows(m: MaskSpec, q0: int, q1: int) -> np.ndarray:
     """Token-level keep mask [q1-q0, L] (uint8) of the block-sparse rule."""
     L = sum(m.side[i] ** 2 for i in range(m.step + 1))

@@ -77,6 +77,15 @@ def test_pruned_restore_pivot_reject_bad_arguments():
     assert L.var_pivot_select(C.byref(p), 12, f, 2048, 819, f, None, f, ws - 1, None) == V.VAR_ERR_WORKSPACE
     assert L.var_pivot_select(C.byref(p), 12, f, 2040, 819, f, None, f, ws, None) == V.VAR_ERR_INVALID_ARG
     assert L.var_pivot_select(C.byref(p), 12, f, 2048, 4097, f, None, f, ws, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_attn_pruned_scatter(C.byref(p), 12, f, f, f, f, 4097, f, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_attn_pruned_scatter(C.byref(p), 12, f, f, f, None, 5, f, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_attn_pruned_scatter(C.byref(p), 12, f, f, f, f, 0, f, None) == V.VAR_OK   # no-op
+    assert L.var_restore_fill(C.byref(p), 0, f, f, 4, f, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_restore_fill(C.byref(p), 12, f, None, 3, f, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_restore_fill(C.byref(p), 12, f, f, -1, f, None) == V.VAR_ERR_INVALID_ARG
+    odd = V.problem(3, 16, 128, SCHEDULE_1024)
+    assert L.var_attn_dense_halved(C.byref(odd), 12, f, f, f, f, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_attn_dense_halved(C.byref(p), 12, f, None, f, f, None) == V.VAR_ERR_INVALID_ARG
 
 
 def _csr_to_token_mask(sides, step, qbs, row_ptr, entries, sink_len):

@@ -108,6 +108,25 @@ def test_dense_split_tail_ctas_every_row():
     check_device_status()
 
 
+@pytest.mark.parametrize("sides,D,B,H", [
+    ((1, 2, 4, 8, 16, 24), 128, 2, 3),     # CFG pair
+    ((1, 2, 3, 5, 7, 11), 64, 4, 2),       # two pairs (cond 0,1 ; uncond 2,3)
+])
+def test_dense_branch_halved(sides, D, B, H):
+    step = len(sides) - 1
+    L, N = cache_len(sides, step), sides[step] ** 2
+    q = randn_bf16((B, H, N, D), 31)
+    k = randn_bf16((B, H, L, D), 32)
+    v = randn_bf16((B, H, L, D), 33)
+    p = V.problem(B, H, D, sides)
+    o = torch.full((B, H, N, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    V.var_attn_dense_halved(p, step, q.to(DEV), k.to(DEV), v.to(DEV), o)
+    torch.cuda.synchronize()
+    assert torch.equal(o[B // 2:], o[: B // 2])                  # the repeat is exact
+    assert_close(o, oracle.branch_halved_attention(q, k, v, L), f"halved {sides}")
+    check_device_status()
+
+
 def test_dense_invariants_on_gpu():
     # identical value rows -> that row; all-equal keys -> mean of values
     B, H, D, sides = 1, 2, 128, (1, 2, 4, 8, 16)

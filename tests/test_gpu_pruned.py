@@ -109,6 +109,47 @@ def test_pivot_single_token_and_large_grid():
     check_device_status()
 
 
+# ---------------------------------------------------------------- fused pruned step
+
+@pytest.mark.parametrize("fill_first", [False, True])
+def test_fused_pruned_step_equals_chain(fill_first):
+    """var_attn_pruned_scatter + var_restore_fill write the same output as
+    var_attn_pruned + var_restore_scatter, bit for bit, in either order."""
+    w = WORKLOADS["pruned_1024px"]
+    inp = make_inputs(w, steps=(12,))
+    step = 12
+    q = inp.q[step]
+    B, H, N, D = q.shape
+    L = cache_len(w.sides, step)
+    K = V.var_keep_count(N, 1, 5)
+    p = V.problem(B, H, D, w.sides)
+    qd, kd, vd = q.to(DEV), inp.k.to(DEV), inp.v.to(DEV)
+    x = inp.x[step].to(DEV)
+    ws = torch.empty(V.var_pivot_workspace_bytes(p, step, x.shape[2]), dtype=torch.uint8, device=DEV)
+    idx = torch.empty((B, K), dtype=torch.int32, device=DEV)
+    V.var_pivot_select(p, step, x, K, idx, ws)
+    prev = randn_bf16((B, H, 48 * 48, D), 77).to(DEV)
+    oc = torch.empty((B, H, K, D), dtype=torch.bfloat16, device=DEV)
+    chain = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=DEV)
+    V.var_attn_pruned(p, step, qd, kd, vd, idx, K, oc)
+    V.var_restore_scatter(p, step, prev, oc, idx, K, chain)
+    fused = torch.full((B, H, N, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    if fill_first:
+        V.var_restore_fill(p, step, prev, idx, K, fused)
+        V.var_attn_pruned_scatter(p, step, qd, kd, vd, idx, K, fused)
+    else:
+        V.var_attn_pruned_scatter(p, step, qd, kd, vd, idx, K, fused)
+        V.var_restore_fill(p, step, prev, idx, K, fused)
+    torch.cuda.synchronize()
+    assert torch.equal(fused, chain)
+    # and against the oracle on sampled kept and upsampled rows
+    ref = oracle.restore_scatter(prev.cpu(), oc.cpu(), idx.cpu().numpy(), 64)
+    rows = sample_rows(B, H, N, 200, seed=3)
+    got = fused.reshape(-1, D)[torch.as_tensor(rows, device=DEV)]
+    assert_close(got, ref.reshape(-1, D)[rows], "fused step")
+    check_device_status()
+
+
 # ---------------------------------------------------------------- pruned attention
 
 @pytest.mark.parametrize("K", [1, 130, 819, 4096])

@@ -45,6 +45,21 @@ def test_attention_matches_bruteforce(sides, D):
             assert np.max(np.abs(got[b, h] - ref)) < 1e-12
 
 
+def test_branch_halved_attention_repeats_the_conditional_half():
+    # the conditional half is the plain attention of those batch elements; the
+    # unconditional half carries the same values, whatever its own inputs
+    sides, B, H, D = (1, 2, 3), 4, 2, 8
+    L, N = 14, 9
+    q = randn_bf16((B, H, N, D), 301)
+    k = randn_bf16((B, H, L, D), 302)
+    v = randn_bf16((B, H, L, D), 303)
+    out = oracle.branch_halved_attention(q, k, v, L)
+    full = oracle.attention(q, k, v, L)
+    assert np.array_equal(out[:2], full[:2])
+    assert np.array_equal(out[2:], full[:2])
+    assert not np.allclose(out[2:], full[2:])       # not the unconditional branch's own attention
+
+
 def test_attention_two_keys_golden():
     g = json.load(open(os.path.join(GOLDEN, "attention_two_keys.json")))
     q = bf(g["q"]).reshape(1, 1, 1, 2)

@@ -65,6 +65,9 @@ _SIGS = {
     "var_pivot_select_noalloc": (C.c_int, [_PROB, C.c_int32, _P, C.c_int32, C.c_int32, _P, _P, _P]),
     "var_attn_pruned": (C.c_int, [_PROB, C.c_int32, _P, _P, _P, _P, C.c_int32, _P, _P]),
     "var_restore_scatter": (C.c_int, [_PROB, C.c_int32, _P, _P, _P, C.c_int32, _P, _P]),
+    "var_attn_pruned_scatter": (C.c_int, [_PROB, C.c_int32, _P, _P, _P, _P, C.c_int32, _P, _P]),
+    "var_restore_fill": (C.c_int, [_PROB, C.c_int32, _P, _P, C.c_int32, _P, _P]),
+    "var_attn_dense_halved": (C.c_int, [_PROB, C.c_int32, _P, _P, _P, _P, _P]),
     "var_block_mask_build": (C.c_int, [_PROB, C.c_int32, C.c_int32, C.c_int32, C.c_int32, _P, _P,
                                        C.c_int32, _P, _P, _P]),
     "var_attn_blocksparse": (C.c_int, [_PROB, C.c_int32, _P, _P, _P,
@@ -166,6 +169,25 @@ def var_attn_pruned(p: var_problem, step: int, q: torch.Tensor, k: torch.Tensor,
     _check("var_attn_pruned", _lib.var_attn_pruned(C.byref(p), step, _ptr(q), _ptr(k), _ptr(v),
                                                    _ptr(idx), keep_k, _ptr(o_compact),
                                                    _stream(stream)))
+
+
+def var_attn_pruned_scatter(p: var_problem, step: int, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                            idx: torch.Tensor, keep_k: int, out: torch.Tensor, stream=None) -> None:
+    _check("var_attn_pruned_scatter",
+           _lib.var_attn_pruned_scatter(C.byref(p), step, _ptr(q), _ptr(k), _ptr(v), _ptr(idx), keep_k,
+                                        _ptr(out), _stream(stream)))
+
+
+def var_restore_fill(p: var_problem, step: int, prev: torch.Tensor, idx: Optional[torch.Tensor], keep_k: int,
+                     out: torch.Tensor, stream=None) -> None:
+    _check("var_restore_fill",
+           _lib.var_restore_fill(C.byref(p), step, _ptr(prev), _ptr(idx), keep_k, _ptr(out), _stream(stream)))
+
+
+def var_attn_dense_halved(p: var_problem, step: int, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                          o: torch.Tensor, stream=None) -> None:
+    _check("var_attn_dense_halved", _lib.var_attn_dense_halved(C.byref(p), step, _ptr(q), _ptr(k), _ptr(v),
+                                                               _ptr(o), _stream(stream)))
 
 
 def var_restore_scatter(p: var_problem, step: int, prev: torch.Tensor, o_compact: Optional[torch.Tensor],

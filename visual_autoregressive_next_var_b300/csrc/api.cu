@@ -144,7 +144,43 @@ int var_attn_pruned(const var_problem* p, int32_t step, const void* q, const voi
     if (!q || !k || !v || !idx || !o_compact) return VAR_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_compact))
         return VAR_ERR_UNSUPPORTED;
-    return launch_attn_pruned(g, q, k, v, idx, keep_k, o_compact, static_cast<cudaStream_t>(stream));
+    return launch_attn_pruned(g, q, k, v, idx, keep_k, o_compact, static_cast<cudaStream_t>(stream), false);
+}
+
+int var_attn_pruned_scatter(const var_problem* p, int32_t step, const void* q, const void* k, const void* v,
+                            const int32_t* idx, int32_t keep_k, void* out, void* stream)
+{
+    StepGeom g;
+    if (int rc = resolve(p, step, &g)) return rc;
+    if (keep_k < 0 || keep_k > g.N) return VAR_ERR_INVALID_ARG;
+    if (keep_k == 0) return VAR_OK;
+    if (!q || !k || !v || !idx || !out) return VAR_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return VAR_ERR_UNSUPPORTED;
+    return launch_attn_pruned(g, q, k, v, idx, keep_k, out, static_cast<cudaStream_t>(stream), true);
+}
+
+int var_restore_fill(const var_problem* p, int32_t step, const void* prev, const int32_t* idx, int32_t keep_k,
+                     void* out, void* stream)
+{
+    StepGeom g;
+    if (int rc = resolve(p, step, &g)) return rc;
+    if (step < 1) return VAR_ERR_INVALID_ARG;
+    if (keep_k < 0 || keep_k > g.N) return VAR_ERR_INVALID_ARG;
+    if (!prev || !out || (keep_k > 0 && !idx)) return VAR_ERR_INVALID_ARG;
+    if (!aligned16(prev) || !aligned16(out)) return VAR_ERR_UNSUPPORTED;
+    return launch_restore_scatter(g.B, g.H, g.D, p->side[step - 1], g.side, prev, nullptr, idx, keep_k, out,
+                                  static_cast<cudaStream_t>(stream), true);
+}
+
+int var_attn_dense_halved(const var_problem* p, int32_t step, const void* q, const void* k, const void* v,
+                          void* o, void* stream)
+{
+    StepGeom g;
+    if (int rc = resolve(p, step, &g)) return rc;
+    if (g.B % 2 != 0) return VAR_ERR_INVALID_ARG;
+    if (!q || !k || !v || !o) return VAR_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return VAR_ERR_UNSUPPORTED;
+    return launch_attn_dense_halved(g, q, k, v, o, static_cast<cudaStream_t>(stream));
 }
 
 int var_restore_scatter(const var_problem* p, int32_t step, const void* prev, const void* o_compact,
@@ -158,7 +194,7 @@ int var_restore_scatter(const var_problem* p, int32_t step, const void* prev, co
     if (!aligned16(prev) || !aligned16(out) || (keep_k > 0 && !aligned16(o_compact)))
         return VAR_ERR_UNSUPPORTED;
     return launch_restore_scatter(g.B, g.H, g.D, p->side[step - 1], g.side, prev, o_compact, idx,
-                                  keep_k, out, static_cast<cudaStream_t>(stream));
+                                  keep_k, out, static_cast<cudaStream_t>(stream), false);
 }
 
 int var_block_mask_build(const var_problem* p, int32_t step, int32_t qblock_side, int32_t radius,

@@ -82,7 +82,8 @@ static TilePlan plan_tiles(int bh, int tiles_per_bh)
 
 template <int D, int MODE>
 static int launch_attn(const StepGeom& g, const void* q, const void* k, const void* v,
-                       const int32_t* idx, int n_rows, void* o, cudaStream_t st)
+                       const int32_t* idx, int n_rows, void* o, cudaStream_t st, bool halved = false,
+                       bool scatter = false)
 {
     using Lay = AttnLayout<D>;
     static bool attr_done = false;   // per process; the attribute is per function
@@ -103,6 +104,8 @@ static int launch_attn(const StepGeom& g, const void* q, const void* k, const vo
     CUtensorMap& tv = maps.v;
     const uint32_t box[3] = {64, 128, 1};
     const uint64_t BH = static_cast<uint64_t>(g.B) * g.H;
+    // branch halving: CTAs cover the first B/2 batch elements (the conditional branch)
+    const uint64_t BH_run = halved ? BH / 2 : BH;
     {
         const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(g.N), BH};
         const uint64_t strides[2] = {D * 2ull, static_cast<uint64_t>(g.N) * D * 2ull};
@@ -121,7 +124,7 @@ static int launch_attn(const StepGeom& g, const void* q, const void* k, const vo
     a.heads = g.H;
     a.tiles_per_bh = (n_rows + 127) / 128;
     a.slots_per_bh = a.tiles_per_bh / 2;
-    const TilePlan plan = plan_tiles(static_cast<int>(BH), a.tiles_per_bh);
+    const TilePlan plan = plan_tiles(static_cast<int>(BH_run), a.tiles_per_bh);
     a.n_pair_ctas = plan.n_pair_ctas;
     a.n_conv_slots = plan.n_conv_slots;
     a.n_kv = (g.L + 127) / 128;
@@ -129,6 +132,8 @@ static int launch_attn(const StepGeom& g, const void* q, const void* k, const vo
     a.q = static_cast<const __nv_bfloat16*>(q);
     a.idx = idx;
     a.o = static_cast<__nv_bfloat16*>(o);
+    a.o_repeat = halved ? static_cast<int64_t>(BH_run) * n_rows * D : 0;
+    a.scatter = scatter ? 1 : 0;
     a.status = status;
     const dim3 grid(static_cast<unsigned>(plan.grid));
     kern<<<grid, 384, Lay::SMEM_BYTES, st>>>(maps, a);
@@ -144,10 +149,18 @@ int launch_attn_dense(const StepGeom& g, const void* q, const void* k, const voi
 }
 
 int launch_attn_pruned(const StepGeom& g, const void* q, const void* k, const void* v,
-                       const int32_t* idx, int keep_k, void* o, cudaStream_t st)
+                       const int32_t* idx, int keep_k, void* o, cudaStream_t st, bool scatter)
 {
-    if (g.D == 128) return launch_attn<128, MODE_GATHER>(g, q, k, v, idx, keep_k, o, st);
-    if (g.D == 64) return launch_attn<64, MODE_GATHER>(g, q, k, v, idx, keep_k, o, st);
+    if (g.D == 128) return launch_attn<128, MODE_GATHER>(g, q, k, v, idx, keep_k, o, st, false, scatter);
+    if (g.D == 64) return launch_attn<64, MODE_GATHER>(g, q, k, v, idx, keep_k, o, st, false, scatter);
+    return VAR_ERR_UNSUPPORTED;
+}
+
+int launch_attn_dense_halved(const StepGeom& g, const void* q, const void* k, const void* v, void* o,
+                             cudaStream_t st)
+{
+    if (g.D == 128) return launch_attn<128, MODE_DENSE>(g, q, k, v, nullptr, g.N, o, st, true);
+    if (g.D == 64) return launch_attn<64, MODE_DENSE>(g, q, k, v, nullptr, g.N, o, st, true);
     return VAR_ERR_UNSUPPORTED;
 }
 

@@ -110,7 +110,11 @@ struct AttnArgs {
     float scale_log2;       // softmax scale * log2(e)
     const __nv_bfloat16* q; // gather source (pruned)
     const int32_t* idx;     // [B][n_rows] (pruned)
-    __nv_bfloat16* o;       // [B][H][n_rows][D]
+    __nv_bfloat16* o;       // [B][H][n_rows][D], or [B][H][n_q][D] when scatter is set
+    int64_t o_repeat;       // non-zero: each output row is also written this many elements further
+                            // (branch halving: the conditional half's rows repeated into the
+                            // unconditional half)
+    int32_t scatter;        // gather mode: write query idx[b][j]'s row of a full-grid output
     int32_t* status;
     // block-sparse
     int32_t side_q;         // query grid side
@@ -561,6 +565,7 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
         const uint32_t tO = tmem + lane_base + (g ? Lay::COL_O1 : Lay::COL_O0);
         const int qrow = row0 + g * 128 + r;
         const int q4 = 2 * g + (r >> 6);     // block of the square (block-sparse); warp-uniform
+        int tok_row = 0;                     // gather mode: the grid token of this query row
 
         if (GATHER && !(split && g == 1)) {
             // This thread's query row, gathered by index, into the swizzled tile.
@@ -570,6 +575,7 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
             if (qrow < args.n_rows) {
                 int tok = __ldg(args.idx + static_cast<size_t>(b) * args.n_rows + qrow);
                 tok = min(max(tok, 0), args.n_q - 1);
+                tok_row = tok;
                 const uint4* src = reinterpret_cast<const uint4*>(
                     args.q + (static_cast<size_t>(bh) * args.n_q + tok) * D);
 #pragma unroll
@@ -731,8 +737,10 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
                     const int y = by * 8 + ((r & 63) >> 3), x = bx * 8 + (r & 7);
                     dst = args.o + (static_cast<size_t>(bh) * args.n_q + y * args.side_q + x) * D;
                 }
-            } else {
-                if (qrow < args.n_rows) dst = args.o + (static_cast<size_t>(bh) * args.n_rows + qrow) * D;
+            } else if (qrow < args.n_rows) {
+                dst = (GATHER && args.scatter)
+                          ? args.o + (static_cast<size_t>(bh) * args.n_q + tok_row) * D
+                          : args.o + (static_cast<size_t>(bh) * args.n_rows + qrow) * D;
             }
             const bool any = l_run > 0.f;            // a row that kept no key is written as zeros
             const float inv = any ? 1.0f / l_run : 0.f;
@@ -760,6 +768,12 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
                     uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) d4[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+                    if (args.o_repeat) {
+                        uint4* r4 = reinterpret_cast<uint4*>(dst + args.o_repeat + c0);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            r4[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+                    }
                 }
             }
         }

@@ -32,7 +32,9 @@ int encode_tmap_bf16(CUtensorMap* out, const void* base, int rank, const uint64_
 int launch_attn_dense(const StepGeom& g, const void* q, const void* k, const void* v, void* o,
                       cudaStream_t st);
 int launch_attn_pruned(const StepGeom& g, const void* q, const void* k, const void* v,
-                       const int32_t* idx, int keep_k, void* o, cudaStream_t st);
+                       const int32_t* idx, int keep_k, void* o, cudaStream_t st, bool scatter);
+int launch_attn_dense_halved(const StepGeom& g, const void* q, const void* k, const void* v, void* o,
+                             cudaStream_t st);
 int launch_attn_blocksparse(const StepGeom& g, const int32_t* sides, int n_scales, int step,
                             const void* q, const void* k, const void* v,
                             const var_block_mask* mask, void* o, cudaStream_t st);
@@ -40,7 +42,7 @@ size_t pivot_workspace_bytes(int B, int N, int C);
 int launch_pivot_select(int B, int N, int C, const void* x, int keep_k, int32_t* idx,
                         float* scores, void* ws, size_t ws_bytes, cudaStream_t st);
 int launch_restore_scatter(int B, int H, int D, int sp, int s, const void* prev, const void* oc,
-                           const int32_t* idx, int keep_k, void* out, cudaStream_t st);
+                           const int32_t* idx, int keep_k, void* out, cudaStream_t st, bool fill_only);
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? VAR_OK : VAR_ERR_CUDA; }
 

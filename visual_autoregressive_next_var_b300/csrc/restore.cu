@@ -1,5 +1,7 @@
 // Structural reconstruction for sm_103a ("ARVAR" Key Design 3, Eq. (8)-(9)):
 //   out = Scatter(Up(prev; s, s), idx, o_compact)
+// In fill mode the kept rows are left as they are (the pruned attention has
+// written them in place) and only the upsampled rows are written.
 // Up is bilinear with half-pixel centres and edge clamp; the scatter overwrites
 // the kept rows.  One pass: every output row is written exactly once, either
 // copied from o_compact (kept token) or blended from four rows of prev.
@@ -32,7 +34,7 @@ template <int D>
 __global__ void __launch_bounds__(256)
     restore_scatter_kernel(const __nv_bfloat16* __restrict__ prev, const __nv_bfloat16* __restrict__ oc,
                            const int32_t* __restrict__ idx, int keep_k, __nv_bfloat16* __restrict__ out,
-                           int H, int sp, int s, float ratio)
+                           int H, int sp, int s, float ratio, int fill_only)
 {
     constexpr int LPT = D / 8;            // lanes per token row (16 B each)
     constexpr int TPW = 32 / LPT;         // token rows per warp step
@@ -65,6 +67,7 @@ __global__ void __launch_bounds__(256)
         const int j = inv[n - n0];
         uint4 r;
         if (j >= 0) {
+            if (fill_only) continue;
             r = __ldg(C + static_cast<size_t>(j) * LPT + part);
         } else {
             const int y = n / s, x = n - y * s;
@@ -96,7 +99,7 @@ __global__ void __launch_bounds__(256)
 }
 
 int launch_restore_scatter(int B, int H, int D, int sp, int s, const void* prev, const void* oc,
-                           const int32_t* idx, int keep_k, void* out, cudaStream_t st)
+                           const int32_t* idx, int keep_k, void* out, cudaStream_t st, bool fill_only)
 {
     const int N = s * s;
     const dim3 grid((N + kRestoreTok - 1) / kRestoreTok, B * H);
@@ -106,9 +109,9 @@ int launch_restore_scatter(int B, int H, int D, int sp, int s, const void* prev,
     auto* C = static_cast<const __nv_bfloat16*>(oc);
     auto* O = static_cast<__nv_bfloat16*>(out);
     if (D == 128)
-        restore_scatter_kernel<128><<<grid, 256, 0, st>>>(P, C, idx, keep_k, O, H, sp, s, ratio);
+        restore_scatter_kernel<128><<<grid, 256, 0, st>>>(P, C, idx, keep_k, O, H, sp, s, ratio, fill_only);
     else if (D == 64)
-        restore_scatter_kernel<64><<<grid, 256, 0, st>>>(P, C, idx, keep_k, O, H, sp, s, ratio);
+        restore_scatter_kernel<64><<<grid, 256, 0, st>>>(P, C, idx, keep_k, O, H, sp, s, ratio, fill_only);
     else
         return VAR_ERR_UNSUPPORTED;
     return cuda_status(cudaGetLastError());
