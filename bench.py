@@ -238,6 +238,7 @@ class Step:
         self.L = cache_len(w.sides, FINAL)
         self.K = V.var_keep_count(self.N, *KEEP)
         self.q = inp.q[FINAL].to(dev)
+        self.q_src = inp.q[FINAL - 3].to(dev)     # the 32x32 step whose attention guides the pivots
         self.k = inp.k.to(dev)
         self.v = inp.v.to(dev)
         self.x = inp.x[FINAL].to(dev)
@@ -402,6 +403,29 @@ def extra_rows(V, dev, step: Step, iters: int, peaks):
                                              "dense_equiv_TFLOP/s": step.flops_dense / t_ov / 1e9,
                                              "timing": "CUDA graph replay after an L2 flush; overlapped = "
                                                        "fill on a second stream beside the attention"}
+    # attention-guided pivots (ARVAR): the 32x32 step's row statistics and saliency
+    src = FINAL - 3
+    B, H, Ns, D = step.q_src.shape
+    o_src = torch.empty_like(step.q_src)
+    lse = torch.empty((B, H, Ns), dtype=torch.float32, device=dev)
+    sal = torch.empty((B, H, Ns), dtype=torch.float32, device=dev)
+    gws = torch.empty(step.V.var_guided_pivot_workspace_bytes(step.p, FINAL), dtype=torch.uint8, device=dev)
+    gidx = torch.empty_like(step.idx)
+    t_plain = time_graph(lambda: step.V.var_attn_dense(step.p, src, step.q_src, step.k, step.v, o_src), iters, flush)
+    t_lse = time_graph(lambda: step.V.var_attn_dense_lse(step.p, src, step.q_src, step.k, step.v, o_src, lse),
+                       iters, flush)
+    t_sal = time_graph(lambda: step.V.var_attn_saliency(step.p, src, step.q_src, step.k, lse, sal), iters, flush)
+    t_sel = time_graph(lambda: step.V.var_guided_pivot_select(step.p, FINAL, src, sal, step.K, gidx, gws),
+                       iters, flush)
+    L_src = cache_len(WORKLOADS[STEP_WORKLOAD].sides, src)
+    fl_sal = 2.0 * B * H * Ns * Ns * D            # S^T = K_self Q^T
+    rows["guided_pivot_from_32x32"] = {
+        "ms": t_sal + t_sel, "saliency_ms": t_sal, "select_ms": t_sel,
+        "saliency_TFLOP/s": fl_sal / t_sal / 1e9,
+        "source_dense_ms": t_plain, "source_dense_with_lse_ms": t_lse,
+        "note": f"source step 32x32 ({Ns} queries, {L_src} keys) -> 64x64, keep 1/5; the row "
+                "statistics are written by the source step's own dense attention",
+        "timing": "CUDA graph replay after an L2 flush"}
     # Branch Halving: the conditional half only, its rows repeated
     t = time_graph(lambda: step.V.var_attn_dense_halved(step.p, FINAL, step.q, step.k, step.v, step.o_dense),
                    iters, flush)
@@ -472,7 +496,7 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     import visual_autoregressive_next_var_b300 as V
 
-    inp = make_inputs(WORKLOADS[STEP_WORKLOAD], steps=(FINAL - 1, FINAL))
+    inp = make_inputs(WORKLOADS[STEP_WORKLOAD], steps=(FINAL - 3, FINAL - 1, FINAL))
     step = Step(V, dev, inp)
     stream = torch.cuda.current_stream(dev)
     flops_equiv = 3.0 * step.flops_dense

@@ -175,6 +175,55 @@ VAR_API int var_restore_fill(const var_problem* p, int32_t step, const void* pre
                              int32_t keep_k, void* out, void* stream);
 
 /*
+ * var_attn_dense that also writes each query row's log2-sum-exp of its scaled
+ * scores, lse[b,h,i] = log2(sum_j 2^(s_ij)), s_ij = Q[b,h,i,:] . K[b,h,j,:] *
+ * scale * log2(e) over the L keys, so that the attention probabilities are
+ * P[i,j] = 2^(s_ij - lse_i).  A step whose attention guides a later step's
+ * pivots ("ARVAR" Key Design 2) keeps these statistics for var_attn_saliency.
+ * lse: [B][H][N] fp32 device (-inf for a row with no key).
+ * Errors: as var_attn_dense.
+ */
+VAR_API int var_attn_dense_lse(const var_problem* p, int32_t step, const void* q, const void* k,
+                               const void* v, void* o, float* lse, void* stream);
+
+/*
+ * Spatial saliency of the source step src_step ("ARVAR" Key Design 2:
+ * attention retrospect -- the self-attention of an earlier, smaller step,
+ * aggregated per position).  For each (b, h) and each token j of the source
+ * grid (the self block: key rows L' - N' .. L' - 1 of the cache at src_step):
+ *   sal[b,h,j] = sum_i P_h[i, L' - N' + j]
+ * the attention probability it receives, summed over the N' source queries,
+ * with the probabilities of var_attn_dense_lse's statistics (softmax over all
+ * L' keys).  The head and query mean is taken by var_guided_pivot_select.
+ * q_src: [B][H][N'][D] (the source step's queries); k: [B][H][kv_capacity][D];
+ * lse: [B][H][N'] from var_attn_dense_lse at src_step; sal: [B][H][N'] fp32.
+ * Errors: as var_attn_dense.
+ */
+VAR_API int var_attn_saliency(const var_problem* p, int32_t src_step, const void* q_src, const void* k,
+                              const float* lse, float* sal, void* stream);
+
+/* Bytes of device workspace var_guided_pivot_select needs (0 on invalid arguments). */
+VAR_API size_t var_guided_pivot_workspace_bytes(const var_problem* p, int32_t step);
+
+/*
+ * Attention-guided pivot selection ("ARVAR" Key Design 2): the head and
+ * query mean of var_attn_saliency's map, v[b, j'] = (1/(H N')) sum_h sal[b,h,j'],
+ * is interpolated bilinearly from the side[src_step] grid to the side[step]
+ * grid (half-pixel centres, edge clamp, as var_restore_scatter), and the
+ * keep_k positions with the largest interpolated value are kept (equal values:
+ * the lower flat index first), written in ascending order.  The values are
+ * computed in fp32 and the ranking is exact on them.
+ * sal: [B][H][side[src_step]^2] fp32; idx: [B][keep_k] int32; scores: optional
+ * [B][side[step]^2] fp32 (the interpolated values) or NULL; workspace of
+ * var_guided_pivot_workspace_bytes() bytes, 256-byte aligned.
+ * Errors: VAR_ERR_INVALID_ARG (src_step >= step, keep_k out of range, null
+ * pointers), VAR_ERR_UNSUPPORTED (more than 16384 tokens), VAR_ERR_WORKSPACE.
+ */
+VAR_API int var_guided_pivot_select(const var_problem* p, int32_t step, int32_t src_step, const float* sal,
+                                    int32_t keep_k, int32_t* idx, float* scores, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+
+/*
  * Dense attention under Branch Halving ("ARVAR" Key Design 1: at a selected
  * step only the conditional branch goes through the block and its output is
  * repeated to restore the two-branch interface).  The batch is the two

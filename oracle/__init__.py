@@ -55,10 +55,15 @@ def lib():
         L.oracle_pivot_select.argtypes = [C.c_int, C.c_int, C.c_int, P, C.c_int, P, P]
         L.oracle_restore_scatter.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, P, P,
                                              P, C.c_int, P]
+        L.oracle_attention_lse.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
+                                           C.c_double, P, P, P]
+        L.oracle_saliency.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
+                                      C.c_double, P, P, P]
         L.oracle_num_threads.restype = C.c_int
         L.oracle_num_threads.argtypes = []
         for f in ("oracle_attention", "oracle_block_mask_rows", "oracle_pivot_mean",
-                  "oracle_pivot_scores", "oracle_pivot_select", "oracle_restore_scatter"):
+                  "oracle_pivot_scores", "oracle_pivot_select", "oracle_restore_scatter",
+                  "oracle_attention_lse", "oracle_saliency"):
             getattr(L, f).restype = C.c_int
         _lib = L
     return _lib
@@ -104,6 +109,73 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, L: int,
     if rc != 0:
         raise ValueError(f"oracle_attention failed ({rc})")
     return out
+
+
+def attention_lse(q: torch.Tensor, k: torch.Tensor, L: int, scale: Optional[float] = None) -> np.ndarray:
+    """Row log2-sum-exp of the scaled scores over the first L keys: [B, H, N] fp64,
+    so that the attention probability is 2^(s_ij log2(e) - lse_i)."""
+    B, H, N, D = q.shape
+    cap = k.shape[2]
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    out = np.zeros((B, H, N), dtype=np.float64)
+    if lib().oracle_attention_lse(B, H, N, L, cap, D, scale, _ptr(_bits(q)), _ptr(_bits(k)), _ptr(out)) != 0:
+        raise ValueError("oracle_attention_lse failed")
+    return out
+
+
+def saliency(q_src: torch.Tensor, k: torch.Tensor, L_src: int, scale: Optional[float] = None) -> np.ndarray:
+    """ARVAR attention retrospect: for each (b, h) and token j of the source grid
+    (key L_src - N' + j, the source step's own scale), the attention probability
+    it receives summed over the N' source queries: [B, H, N'] fp64."""
+    B, H, N, D = q_src.shape
+    cap = k.shape[2]
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    out = np.zeros((B, H, N), dtype=np.float64)
+    if lib().oracle_saliency(B, H, N, L_src, cap, D, scale, _ptr(_bits(q_src)), _ptr(_bits(k)), _ptr(out)) != 0:
+        raise ValueError("oracle_saliency failed")
+    return out
+
+
+def bilinear_map(m: np.ndarray, side: int) -> np.ndarray:
+    """Bilinear upsampling of [..., sp*sp] maps to [..., side*side] in fp64: half-pixel
+    centres, edge clamp, no antialias (the restore's convention)."""
+    sp = int(round(m.shape[-1] ** 0.5))
+    assert sp * sp == m.shape[-1]
+
+    def axis(n_out):
+        dst = np.arange(n_out, dtype=np.float64)
+        src = np.maximum((dst + 0.5) * sp / n_out - 0.5, 0.0)
+        i0 = np.minimum(np.floor(src).astype(np.int64), sp - 1)
+        i1 = np.minimum(i0 + 1, sp - 1)
+        return i0, i1, src - i0
+
+    y0, y1, ly = axis(side)
+    x0, x1, lx = axis(side)
+    g = m.reshape(m.shape[:-1] + (sp, sp))
+    ly = ly[:, None]
+    lx = lx[None, :]
+    top = g[..., y0[:, None], x0[None, :]] * (1 - lx) + g[..., y0[:, None], x1[None, :]] * lx
+    bot = g[..., y1[:, None], x0[None, :]] * (1 - lx) + g[..., y1[:, None], x1[None, :]] * lx
+    return (top * (1 - ly) + bot * ly).reshape(m.shape[:-1] + (side * side,))
+
+
+def top_k_ascending(values: np.ndarray, keep_k: int) -> np.ndarray:
+    """Per row of [B, N]: the keep_k largest (equal values: lower index first), ascending."""
+    B, N = values.shape
+    out = np.zeros((B, keep_k), dtype=np.int32)
+    for b in range(B):
+        order = sorted(range(N), key=lambda i: (-values[b, i], i))
+        out[b] = np.sort(np.array(order[:keep_k], dtype=np.int32))
+    return out
+
+
+def guided_pivot(sal: np.ndarray, side: int, keep_k: int):
+    """ARVAR attention-guided pivots: the head and query mean of the per-head
+    saliency sums [B, H, N'], bilinearly upsampled to side x side, Top-K.
+    Returns (idx [B, K] ascending, values [B, side*side])."""
+    B, H, Np = sal.shape
+    v = bilinear_map(sal.sum(axis=1) / (H * Np), side)
+    return top_k_ascending(v, keep_k), v
 
 
 def branch_halved_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, L: int,

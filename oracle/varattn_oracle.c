@@ -203,6 +203,89 @@ int oracle_attention(int B, int H, int N, int L, int kv_cap, int D, double scale
 }
 
 /* ------------------------------------------------------------------ */
+/* Attention retrospect (ARVAR Key Design 2): row statistics and the   */
+/* probability each token of the source grid receives                  */
+/* ------------------------------------------------------------------ */
+
+/* s_j = q . k_j * scale for j < L; returns the maximum. */
+static double row_scores(int L, int D, double scale, const uint16_t* q, const uint16_t* K, double* s)
+{
+    double mx = -INFINITY;
+    for (int j = 0; j < L; j++) {
+        double dot = 0.0;
+        for (int d = 0; d < D; d++) dot += bf16_to_f64(q[d]) * bf16_to_f64(K[(size_t)j * D + d]);
+        s[j] = dot * scale;
+        if (s[j] > mx) mx = s[j];
+    }
+    return mx;
+}
+
+/*
+ * lse[bh][i] = log2(sum_j e^(s_ij)), s_ij = q_i . k_j * scale over the first L
+ * keys, so that the attention probability is 2^(s_ij log2(e) - lse_i).
+ */
+int oracle_attention_lse(int B, int H, int N, int L, int kv_cap, int D, double scale,
+                         const uint16_t* q, const uint16_t* k, double* lse)
+{
+    if (B <= 0 || H <= 0 || N <= 0 || L <= 0 || D <= 0 || kv_cap < L) return 1;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)L);
+        if (!s) {
+#pragma omp atomic write
+            bad = 2;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (long flat = 0; flat < (long)B * H * N; flat++) {
+                const long bh = flat / N;
+                const double mx = row_scores(L, D, scale, q + (size_t)flat * D, k + (size_t)bh * kv_cap * D, s);
+                double l = 0.0;
+                for (int j = 0; j < L; j++) l += exp(s[j] - mx);
+                lse[flat] = (mx + log(l)) / log(2.0);
+            }
+            free(s);
+        }
+    }
+    return bad;
+}
+
+/*
+ * sal[bh][j] = sum_i P[i, L - N + j]: the softmax probability (over all L keys)
+ * that key L - N + j of the self block -- token j of the N-token source grid --
+ * receives from each of the N source queries, summed over the queries.
+ */
+int oracle_saliency(int B, int H, int N, int L, int kv_cap, int D, double scale,
+                    const uint16_t* q, const uint16_t* k, double* sal)
+{
+    if (B <= 0 || H <= 0 || N <= 0 || L < N || D <= 0 || kv_cap < L) return 1;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)L);
+        if (!s) {
+#pragma omp atomic write
+            bad = 2;
+        } else {
+#pragma omp for schedule(static)
+            for (long bh = 0; bh < (long)B * H; bh++) {
+                double* out = sal + (size_t)bh * N;
+                for (int j = 0; j < N; j++) out[j] = 0.0;
+                for (int i = 0; i < N; i++) {
+                    const double mx = row_scores(L, D, scale, q + ((size_t)bh * N + i) * D,
+                                                 k + (size_t)bh * kv_cap * D, s);
+                    double l = 0.0;
+                    for (int j = 0; j < L; j++) l += exp(s[j] - mx);
+                    for (int j = 0; j < N; j++) out[j] += exp(s[L - N + j] - mx) / l;
+                }
+            }
+            free(s);
+        }
+    }
+    return bad;
+}
+
+/* ------------------------------------------------------------------ */
 /* Pivot score + top-K (FastVAR cached token pruning)                  */
 /* ------------------------------------------------------------------ */
 

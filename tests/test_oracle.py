@@ -45,6 +45,57 @@ def test_attention_matches_bruteforce(sides, D):
             assert np.max(np.abs(got[b, h] - ref)) < 1e-12
 
 
+# ---------------------------------------------------------------- attention retrospect (ARVAR)
+
+def _np_bits(t):
+    return t.float().double().numpy()
+
+
+def test_attention_lse_and_saliency_match_bruteforce():
+    B, H, D = 2, 2, 16
+    sides = (2, 3)                       # cache: 4 + 9 tokens; the source grid is the 3x3 scale
+    L, N = 13, 9
+    q = randn_bf16((B, H, N, D), 311)
+    k = randn_bf16((B, H, L, D), 312)
+    scale = 1.0 / np.sqrt(D)
+    s = np.einsum("bhnd,bhld->bhnl", _np_bits(q), _np_bits(k)) * scale
+    lse_ref = np.log2(np.exp(s).sum(-1))
+    assert np.allclose(oracle.attention_lse(q, k, L), lse_ref, rtol=0, atol=1e-12)
+    P = np.exp(s - s.max(-1, keepdims=True))
+    P /= P.sum(-1, keepdims=True)
+    sal_ref = P[..., L - N:].sum(axis=2)               # per (b, h, source key): sum over queries
+    assert np.allclose(oracle.saliency(q, k, L), sal_ref, rtol=0, atol=1e-12)
+
+
+def test_saliency_closed_forms():
+    B, H, D, N, L = 1, 2, 8, 16, 21
+    zero_q = torch.zeros((B, H, N, D), dtype=torch.bfloat16)
+    k = randn_bf16((B, H, L, D), 313)
+    # zero queries: every key gets 1/L from every query
+    assert np.allclose(oracle.saliency(zero_q, k, L), N / L, rtol=0, atol=1e-12)
+    # a cache that is only the source scale: each query's mass (1) all lands in it
+    q = randn_bf16((B, H, N, D), 314)
+    kk = randn_bf16((B, H, N, D), 315)
+    assert np.allclose(oracle.saliency(q, kk, N).sum(-1), N, rtol=0, atol=1e-9)
+
+
+@pytest.mark.parametrize("sp,s", [(3, 5), (4, 8), (32, 64), (5, 5), (7, 3)])
+def test_bilinear_map_matches_library_interpolate(sp, s):
+    m = np.random.default_rng(sp * 100 + s).standard_normal((2, sp * sp))
+    ref = torch.nn.functional.interpolate(torch.from_numpy(m).reshape(2, 1, sp, sp), size=(s, s),
+                                          mode="bilinear", align_corners=False).reshape(2, s * s).numpy()
+    assert np.allclose(oracle.bilinear_map(m, s), ref, rtol=0, atol=1e-12)
+
+
+def test_top_k_ascending_ties_and_order():
+    v = np.array([[1.0, 3.0, 3.0, 2.0, 3.0, 0.5]])
+    assert np.array_equal(oracle.top_k_ascending(v, 2), [[1, 2]])      # ties: lower index first
+    assert np.array_equal(oracle.top_k_ascending(v, 4), [[1, 2, 3, 4]])
+    assert np.array_equal(oracle.top_k_ascending(np.zeros((2, 7)), 3), [[0, 1, 2], [0, 1, 2]])
+    idx, vals = oracle.guided_pivot(np.ones((2, 3, 4)), 4, 5)            # constant map: all tie
+    assert np.array_equal(idx, [[0, 1, 2, 3, 4]] * 2) and np.allclose(vals, 1.0 / 4)
+
+
 def test_branch_halved_attention_repeats_the_conditional_half():
     # the conditional half is the plain attention of those batch elements; the
     # unconditional half carries the same values, whatever its own inputs

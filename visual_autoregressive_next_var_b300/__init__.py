@@ -68,6 +68,11 @@ _SIGS = {
     "var_attn_pruned_scatter": (C.c_int, [_PROB, C.c_int32, _P, _P, _P, _P, C.c_int32, _P, _P]),
     "var_restore_fill": (C.c_int, [_PROB, C.c_int32, _P, _P, C.c_int32, _P, _P]),
     "var_attn_dense_halved": (C.c_int, [_PROB, C.c_int32, _P, _P, _P, _P, _P]),
+    "var_attn_dense_lse": (C.c_int, [_PROB, C.c_int32, _P, _P, _P, _P, _P, _P]),
+    "var_attn_saliency": (C.c_int, [_PROB, C.c_int32, _P, _P, _P, _P, _P]),
+    "var_guided_pivot_workspace_bytes": (C.c_size_t, [_PROB, C.c_int32]),
+    "var_guided_pivot_select": (C.c_int, [_PROB, C.c_int32, C.c_int32, _P, C.c_int32, _P, _P, _P, C.c_size_t,
+                                          _P]),
     "var_block_mask_build": (C.c_int, [_PROB, C.c_int32, C.c_int32, C.c_int32, C.c_int32, _P, _P,
                                        C.c_int32, _P, _P, _P]),
     "var_attn_blocksparse": (C.c_int, [_PROB, C.c_int32, _P, _P, _P,
@@ -188,6 +193,31 @@ def var_attn_dense_halved(p: var_problem, step: int, q: torch.Tensor, k: torch.T
                           o: torch.Tensor, stream=None) -> None:
     _check("var_attn_dense_halved", _lib.var_attn_dense_halved(C.byref(p), step, _ptr(q), _ptr(k), _ptr(v),
                                                                _ptr(o), _stream(stream)))
+
+
+def var_attn_dense_lse(p: var_problem, step: int, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                       o: torch.Tensor, lse: torch.Tensor, stream=None) -> None:
+    _check("var_attn_dense_lse", _lib.var_attn_dense_lse(C.byref(p), step, _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                                         _ptr(lse), _stream(stream)))
+
+
+def var_attn_saliency(p: var_problem, src_step: int, q_src: torch.Tensor, k: torch.Tensor, lse: torch.Tensor,
+                      sal: torch.Tensor, stream=None) -> None:
+    _check("var_attn_saliency", _lib.var_attn_saliency(C.byref(p), src_step, _ptr(q_src), _ptr(k), _ptr(lse),
+                                                       _ptr(sal), _stream(stream)))
+
+
+def var_guided_pivot_workspace_bytes(p: var_problem, step: int) -> int:
+    return _lib.var_guided_pivot_workspace_bytes(C.byref(p), step)
+
+
+def var_guided_pivot_select(p: var_problem, step: int, src_step: int, sal: torch.Tensor, keep_k: int,
+                            idx: Optional[torch.Tensor], workspace: torch.Tensor,
+                            scores: Optional[torch.Tensor] = None, stream=None) -> None:
+    _check("var_guided_pivot_select",
+           _lib.var_guided_pivot_select(C.byref(p), step, src_step, _ptr(sal), keep_k, _ptr(idx), _ptr(scores),
+                                        _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                        _stream(stream)))
 
 
 def var_restore_scatter(p: var_problem, step: int, prev: torch.Tensor, o_compact: Optional[torch.Tensor],

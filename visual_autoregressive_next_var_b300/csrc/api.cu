@@ -172,6 +172,49 @@ int var_restore_fill(const var_problem* p, int32_t step, const void* prev, const
                                   static_cast<cudaStream_t>(stream), true);
 }
 
+int var_attn_dense_lse(const var_problem* p, int32_t step, const void* q, const void* k, const void* v, void* o,
+                       float* lse, void* stream)
+{
+    StepGeom g;
+    if (int rc = resolve(p, step, &g)) return rc;
+    if (!q || !k || !v || !o || !lse) return VAR_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return VAR_ERR_UNSUPPORTED;
+    return launch_attn_dense(g, q, k, v, o, static_cast<cudaStream_t>(stream), lse);
+}
+
+int var_attn_saliency(const var_problem* p, int32_t src_step, const void* q_src, const void* k, const float* lse,
+                      float* sal, void* stream)
+{
+    StepGeom g;
+    if (int rc = resolve(p, src_step, &g)) return rc;
+    if (!q_src || !k || !lse || !sal) return VAR_ERR_INVALID_ARG;
+    if (!aligned16(q_src) || !aligned16(k)) return VAR_ERR_UNSUPPORTED;
+    return launch_saliency(g, g.N, g.L, q_src, k, lse, sal, static_cast<cudaStream_t>(stream));
+}
+
+size_t var_guided_pivot_workspace_bytes(const var_problem* p, int32_t step)
+{
+    StepGeom g;
+    if (resolve(p, step, &g) != VAR_OK) return 0;
+    return guided_workspace_bytes(g.B, g.N);
+}
+
+int var_guided_pivot_select(const var_problem* p, int32_t step, int32_t src_step, const float* sal,
+                            int32_t keep_k, int32_t* idx, float* scores, void* workspace, size_t workspace_bytes,
+                            void* stream)
+{
+    StepGeom g;
+    if (int rc = resolve(p, step, &g)) return rc;
+    if (src_step < 0 || src_step >= step) return VAR_ERR_INVALID_ARG;
+    if (!sal || keep_k < 0 || keep_k > g.N || (keep_k > 0 && !idx)) return VAR_ERR_INVALID_ARG;
+    if (g.N > 16384) return VAR_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < guided_workspace_bytes(g.B, g.N) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return VAR_ERR_WORKSPACE;
+    return launch_guided_pivot(g.B, g.H, p->side[src_step], g.side, sal, keep_k, idx, scores, workspace,
+                               workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
 int var_attn_dense_halved(const var_problem* p, int32_t step, const void* q, const void* k, const void* v,
                           void* o, void* stream)
 {

@@ -83,7 +83,7 @@ static TilePlan plan_tiles(int bh, int tiles_per_bh)
 template <int D, int MODE>
 static int launch_attn(const StepGeom& g, const void* q, const void* k, const void* v,
                        const int32_t* idx, int n_rows, void* o, cudaStream_t st, bool halved = false,
-                       bool scatter = false)
+                       bool scatter = false, float* lse = nullptr)
 {
     using Lay = AttnLayout<D>;
     static bool attr_done = false;   // per process; the attribute is per function
@@ -134,6 +134,7 @@ static int launch_attn(const StepGeom& g, const void* q, const void* k, const vo
     a.o = static_cast<__nv_bfloat16*>(o);
     a.o_repeat = halved ? static_cast<int64_t>(BH_run) * n_rows * D : 0;
     a.scatter = scatter ? 1 : 0;
+    a.lse = lse;
     a.status = status;
     const dim3 grid(static_cast<unsigned>(plan.grid));
     kern<<<grid, 384, Lay::SMEM_BYTES, st>>>(maps, a);
@@ -141,10 +142,10 @@ static int launch_attn(const StepGeom& g, const void* q, const void* k, const vo
 }
 
 int launch_attn_dense(const StepGeom& g, const void* q, const void* k, const void* v, void* o,
-                      cudaStream_t st)
+                      cudaStream_t st, float* lse)
 {
-    if (g.D == 128) return launch_attn<128, MODE_DENSE>(g, q, k, v, nullptr, g.N, o, st);
-    if (g.D == 64) return launch_attn<64, MODE_DENSE>(g, q, k, v, nullptr, g.N, o, st);
+    if (g.D == 128) return launch_attn<128, MODE_DENSE>(g, q, k, v, nullptr, g.N, o, st, false, false, lse);
+    if (g.D == 64) return launch_attn<64, MODE_DENSE>(g, q, k, v, nullptr, g.N, o, st, false, false, lse);
     return VAR_ERR_UNSUPPORTED;
 }
 

@@ -115,6 +115,8 @@ struct AttnArgs {
                             // (branch halving: the conditional half's rows repeated into the
                             // unconditional half)
     int32_t scatter;        // gather mode: write query idx[b][j]'s row of a full-grid output
+    float* lse;             // dense mode, optional: [B][H][n_rows] row log2-sum-exp of the scaled
+                            // scores (log2 of sum_j 2^(s_ij * scale * log2 e))
     int32_t* status;
     // block-sparse
     int32_t side_q;         // query grid side
@@ -723,6 +725,7 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
                 a0 = l_run > 0.f ? ex2_approx(m_run - mm) : 0.f;
                 a1 = ml.y > 0.f ? ex2_approx(ml.x - mm) : 0.f;
                 l_run = l_run * a0 + ml.y * a1;
+                m_run = mm;
             }
         }
         if (!ok) {
@@ -744,6 +747,8 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
             }
             const bool any = l_run > 0.f;            // a row that kept no key is written as zeros
             const float inv = any ? 1.0f / l_run : 0.f;
+            if (!SPARSE && !GATHER && args.lse && qrow < args.n_rows)
+                args.lse[static_cast<size_t>(bh) * args.n_rows + qrow] = any ? m_run + log2f(l_run) : -INFINITY;
             const uint32_t tO1 = tmem + lane_base + Lay::COL_O1;
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {

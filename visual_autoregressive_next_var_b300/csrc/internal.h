@@ -30,7 +30,7 @@ int encode_tmap_bf16(CUtensorMap* out, const void* base, int rank, const uint64_
                      const uint64_t* strides_bytes, const uint32_t* box);
 
 int launch_attn_dense(const StepGeom& g, const void* q, const void* k, const void* v, void* o,
-                      cudaStream_t st);
+                      cudaStream_t st, float* lse = nullptr);
 int launch_attn_pruned(const StepGeom& g, const void* q, const void* k, const void* v,
                        const int32_t* idx, int keep_k, void* o, cudaStream_t st, bool scatter);
 int launch_attn_dense_halved(const StepGeom& g, const void* q, const void* k, const void* v, void* o,
@@ -41,6 +41,13 @@ int launch_attn_blocksparse(const StepGeom& g, const int32_t* sides, int n_scale
 size_t pivot_workspace_bytes(int B, int N, int C);
 int launch_pivot_select(int B, int N, int C, const void* x, int keep_k, int32_t* idx,
                         float* scores, void* ws, size_t ws_bytes, cudaStream_t st);
+int launch_select_exact(int B, int N, int keep_k, const float* keys_lo, const float* keys_hi, int* band_idx,
+                        double* band_score, int32_t* idx, cudaStream_t st);
+int launch_saliency(const StepGeom& g, int n_src, int L_src, const void* q, const void* k, const float* lse,
+                    float* sal, cudaStream_t st);
+size_t guided_workspace_bytes(int B, int N);
+int launch_guided_pivot(int B, int H, int sp, int s, const float* sal, int keep_k, int32_t* idx, float* scores,
+                        void* ws, size_t ws_bytes, cudaStream_t st);
 int launch_restore_scatter(int B, int H, int D, int sp, int s, const void* prev, const void* oc,
                            const int32_t* idx, int keep_k, void* out, cudaStream_t st, bool fill_only);
 

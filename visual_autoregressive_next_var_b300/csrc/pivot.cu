@@ -738,7 +738,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     pivot_select_kernel(const __nv_bfloat16* __restrict__ x, int N, int C, int K, const float* __restrict__ lo_g,
                         const float* __restrict__ hi_g, const double* __restrict__ mean64,
                         int* __restrict__ band_idx_g, double* __restrict__ band_score_g,
-                        int32_t* __restrict__ idx_out, int32_t* status)
+                        int32_t* __restrict__ idx_out, int32_t* status, int exact)
 {
     __shared__ SelShared S;
     const int b = blockIdx.x;
@@ -811,7 +811,8 @@ __global__ void __launch_bounds__(kSelThreads, 1)
         }
         return;
     }
-    // fp64 re-score of the band in the exact evaluation order
+    // the band's exact scores: fp64 re-score in the exact evaluation order, or
+    // (exact keys, lo = hi) the key value itself
     int* band_idx = band_idx_g + static_cast<size_t>(b) * N;
     double* band_score = band_score_g + static_cast<size_t>(b) * N;
 #pragma unroll
@@ -820,15 +821,20 @@ __global__ void __launch_bounds__(kSelThreads, 1)
         if ((fband >> k) & 1u) band_idx[(S.blk[k * kSelWarps + warp] & 0xFFFF) + __popc(mb & lt)] = tid + kSelThreads * k;
     }
     __syncthreads();
-    const int q = C / 32;
-    const double* mb64 = mean64 + static_cast<size_t>(b) * C;
-    for (int j = warp; j < tot_band; j += kSelWarps) {
-        const int i = band_idx[j];
-        const __nv_bfloat16* row = x + (static_cast<size_t>(b) * N + i) * C;
-        double v = tree64(row + lane * q, mb64 + lane * q, q);
+    if (exact) {
+        for (int j = tid; j < tot_band; j += kSelThreads)
+            band_score[j] = static_cast<double>(__ldcg(lo_g + static_cast<size_t>(b) * N + band_idx[j]));
+    } else {
+        const int q = C / 32;
+        const double* mb64 = mean64 + static_cast<size_t>(b) * C;
+        for (int j = warp; j < tot_band; j += kSelWarps) {
+            const int i = band_idx[j];
+            const __nv_bfloat16* row = x + (static_cast<size_t>(b) * N + i) * C;
+            double v = tree64(row + lane * q, mb64 + lane * q, q);
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) v = __dadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
-        if (lane == 0) band_score[j] = v;
+            for (int off = 1; off < 32; off <<= 1) v = __dadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
+            if (lane == 0) band_score[j] = v;
+        }
     }
     __syncthreads();
     for (int j = tid; j < tot_band; j += kSelThreads) {
@@ -937,10 +943,24 @@ int launch_pivot_select(int B, int N, int C, const void* xv, int keep_k, int32_t
                                           : pivot_select_kernel<kMaxKeysPerThread>;
         if (cudaLaunchKernelEx(&cfg, fn, x, N, C, keep_k, static_cast<const float*>(lok),
                                static_cast<const float*>(hik), static_cast<const double*>(m64), bidx, bsc, idx,
-                               status) != cudaSuccess)
+                               status, 0) != cudaSuccess)
             return VAR_ERR_CUDA;
     }
     return VAR_OK;
+}
+
+int launch_select_exact(int B, int N, int keep_k, const float* keys_lo, const float* keys_hi, int* band_idx,
+                        double* band_score, int32_t* idx, cudaStream_t st)
+{
+    if (N > kMaxN) return VAR_ERR_UNSUPPORTED;
+    int32_t* status = device_status_ptr();
+    if (!status) return VAR_ERR_CUDA;
+    auto* fn = N <= 4 * kSelThreads ? pivot_select_kernel<4>
+               : N <= 8 * kSelThreads ? pivot_select_kernel<8>
+                                      : pivot_select_kernel<kMaxKeysPerThread>;
+    fn<<<B, kSelThreads, 0, st>>>(nullptr, N, 32, keep_k, keys_lo, keys_hi, nullptr, band_idx, band_score, idx,
+                                  status, 1);
+    return cuda_status(cudaGetLastError());
 }
 
 // ---------------------------------------------------------------------------
