@@ -39,7 +39,8 @@ struct SalLayout {
     static constexpr int NSQ = 2;                      // query tile ring
     static constexpr int OFF_K = 0;                    // the CTA's 128 keys (A operand)
     static constexpr int OFF_Q = OFF_K + TILE_BYTES;   // query tiles (B operand)
-    static constexpr int OFF_BAR = OFF_Q + NSQ * TILE_BYTES;
+    static constexpr int OFF_LSE = OFF_Q + NSQ * TILE_BYTES;   // [4 warps][128] float, warp-private
+    static constexpr int OFF_BAR = OFF_LSE + 4 * 128 * 4;
     static constexpr int B_KF = 0;                     // key tile resident
     static constexpr int B_QF = 1;                     // [NSQ] query slot full
     static constexpr int B_QE = B_QF + NSQ;            // [NSQ] query slot free
@@ -173,9 +174,10 @@ __global__ void __launch_bounds__(256, 2) saliency_kernel(const __grid_constant_
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ consumers: one key row each
-        // The query statistics are read straight from global memory: every lane of
-        // a warp loads the same value (one broadcast transaction, L1-resident).
+        // Each warp stages a tile's 128 query statistics in its own slice of shared
+        // memory (4 per lane) and reads them back as broadcast 16-byte loads.
         const int r = (warp & 3) * 32 + lane;
+        float* lw = reinterpret_cast<float*>(smem + Lay::OFF_LSE) + (warp & 3) * 128;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const float sl2 = a.scale_log2;
         const float* lse_bh = a.lse + static_cast<size_t>(bh) * a.n_src;
@@ -189,26 +191,27 @@ __global__ void __launch_bounds__(256, 2) saliency_kernel(const __grid_constant_
                 break;
             }
             tc_fence_after();
-            const bool full = q0 + 128 <= a.n_src;
+            __syncwarp();                              // the previous tile's reads are done
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {              // columns past N': probability 0
+                const int qi = q0 + lane * 4 + e;
+                lw[lane * 4 + e] = qi < a.n_src ? __ldg(lse_bh + qi) : INFINITY;
+            }
+            __syncwarp();
 #pragma unroll
             for (int c0 = 0; c0 < 128; c0 += 32) {
-                float lv[32];
-                if (full) {
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) lv[c] = __ldg(lse_bh + q0 + c0 + c);
-                } else {                               // columns past N': probability 0
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        lv[c] = q0 + c0 + c < a.n_src ? __ldg(lse_bh + q0 + c0 + c) : INFINITY;
-                }
                 uint32_t sv[32];
                 tmem_ld32(tmem + lane_base + static_cast<uint32_t>(buf * 128 + c0), sv);
                 tmem_wait_ld();
 #pragma unroll
-                for (int c = 0; c < 32; c += 2) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(sv[c]), sl2, -lv[c]));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(sv[c + 1]), sl2, -lv[c + 1]));
+                for (int c = 0; c < 32; c += 4) {
+                    const float4 l4 = *reinterpret_cast<const float4*>(lw + c0 + c);
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(sv[c]), sl2, -l4.x));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(sv[c + 1]), sl2, -l4.y));
+                    const float p2 = ex2_approx(fmaf(__uint_as_float(sv[c + 2]), sl2, -l4.z));
+                    const float p3 = ex2_approx(fmaf(__uint_as_float(sv[c + 3]), sl2, -l4.w));
                     acc2 = f2_add(acc2, f2_pack(p0, p1));
+                    acc2 = f2_add(acc2, f2_pack(p2, p3));
                 }
             }
             tc_fence_before();
