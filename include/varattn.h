@@ -273,6 +273,13 @@ typedef struct {
     int32_t nnz;           /* entries[] length */
     const int32_t* row_ptr;  /* device [n_qblocks + 1] */
     const int32_t* entries;  /* device [nnz] */
+    /* Optional kernel plan (device copies of var_block_mask_plan's output), or
+       n_squares = 0 and NULL pointers: the kernel then merges the lists itself. */
+    int32_t n_squares;       /* ceil(side / qblock_side / 2)^2 */
+    int32_t plan_units;      /* sq_ptr[n_squares]: units in sq_units */
+    const int32_t* sq_ptr;   /* device [n_squares + 1] */
+    const int32_t* sq_units; /* device [2 * sq_ptr[n_squares]] */
+    const int32_t* sq_order; /* device [n_squares] */
 } var_block_mask;
 
 /*
@@ -286,6 +293,27 @@ VAR_API int var_block_mask_build(const var_problem* p, int32_t step, int32_t qbl
                          int32_t radius, int32_t sink_max_side, int32_t* row_ptr,
                          int32_t* entries, int32_t entries_cap, int32_t* nnz_out,
                          int32_t* n_qblocks_out, int32_t* sink_len_out);
+
+/*
+ * Build, on the HOST, the block-sparse kernel's plan for a mask: the kernel
+ * runs one CTA per 2 x 2 square of query blocks over the union of the four
+ * blocks' key lists.  The plan holds, per square, that union as the kernel's
+ * 64-key units (the sink range in 64-token chunks, then the key blocks in
+ * ascending order, each with the set of the square's blocks that keep it and
+ * its extent at the scale edge; the encoding is the library's own), and the
+ * order in which CTAs take the squares (most units first).  The mask depends
+ * only on the schedule, so the plan is built once and reused; without it the
+ * kernel merges the four lists in every CTA.
+ * row_ptr / entries: var_block_mask_build's host output; sq_ptr: [n_squares+1];
+ * sq_units: 2 * units_cap ints; sq_order: [n_squares] (host).  Call with
+ * sq_units = NULL to get *n_squares_out and *n_units_out for sizing.
+ * Errors: VAR_ERR_INVALID_ARG (sizes, malformed entries), VAR_ERR_UNSUPPORTED
+ * (qblock_side other than 8, a square with more than 1024 units).
+ */
+VAR_API int var_block_mask_plan(const var_problem* p, int32_t step, int32_t qblock_side,
+                                const int32_t* row_ptr, const int32_t* entries, int32_t sink_len,
+                                int32_t* sq_ptr, int32_t* sq_units, int32_t units_cap, int32_t* sq_order,
+                                int32_t* n_squares_out, int32_t* n_units_out);
 
 /*
  * Block-sparse cross-scale attention: as var_attn_dense, but query i of block

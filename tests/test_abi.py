@@ -152,6 +152,42 @@ def test_block_mask_2k_statistics_and_rows():
         assert np.array_equal(keys, ref)
 
 
+@pytest.mark.parametrize("sides,radius,sink", [
+    (SCHEDULE_2K, 2, 16),
+    ((1, 2, 4, 8, 16, 24, 40), 2, 4),          # 5x5 query blocks: squares at the edge are partial
+])
+def test_block_mask_plan_is_the_union_of_each_square(sides, radius, sink):
+    step = len(sides) - 1
+    p = V.problem(2, 16, 128, sides)
+    rp, en, sink_len = V.var_block_mask_build(p, step, 8, radius, sink)
+    sq_ptr, sq_units, sq_order = V.var_block_mask_plan(p, step, 8, rp, en, sink_len)
+    nb = sides[step] // 8
+    nsq = (nb + 1) // 2
+    n_sink = (sink_len + 63) // 64
+    assert len(sq_order) == nsq * nsq and sorted(sq_order.tolist()) == list(range(nsq * nsq))
+    counts = np.diff(sq_ptr)
+    assert all(counts[sq_order[i]] >= counts[sq_order[i + 1]] for i in range(len(sq_order) - 1))
+    for sq in range(nsq * nsq):
+        by0, bx0 = 2 * (sq // nsq), 2 * (sq % nsq)
+        member = {}
+        for t in range(4):
+            by, bx = by0 + t // 2, bx0 + t % 2
+            if by < nb and bx < nb:
+                qb = by * nb + bx
+                for e in en[rp[qb]:rp[qb + 1]]:
+                    member[int(e)] = member.get(int(e), 0) | (1 << t)
+        units = sq_units[2 * sq_ptr[sq]: 2 * sq_ptr[sq + 1]].reshape(-1, 2)
+        assert len(units) == n_sink + len(member)
+        assert [int(u) for u in units[:n_sink, 0]] == [-1 - c for c in range(n_sink)]
+        assert [int(u) for u in units[n_sink:, 0]] == sorted(member)
+        for e, meta in units[n_sink:]:
+            s = sides[int(e) >> 24]
+            u, v = (int(e) >> 12) & 0xFFF, int(e) & 0xFFF
+            rows, cols = min(8, s - 8 * u), min(8, s - 8 * v)
+            assert int(meta) & 0xF == member[int(e)]
+            assert (int(meta) >> 8) & 15 == rows and (int(meta) >> 12) & 15 == cols
+
+
 def test_block_mask_rejects_bad_shapes():
     p = V.problem(1, 1, 64, (1, 2, 4, 6, 8, 12, 16, 20))
     with pytest.raises(V.VarError):

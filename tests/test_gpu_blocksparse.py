@@ -45,6 +45,35 @@ def test_blocksparse_small_full(sides, D, B, H, radius, sink):
     check_device_status()
 
 
+@pytest.mark.parametrize("sides,D,B,H,radius,sink", [
+    ((1, 2, 4, 6, 8, 12, 16, 20, 24, 32), 128, 2, 2, 1, 8),
+    ((1, 2, 4, 8, 16, 24, 40), 128, 1, 2, 2, 4),             # partial squares at the edge
+    ((1, 2, 4, 6, 8, 12, 16, 20, 24, 32, 40, 48, 64), 64, 1, 2, 2, 16),
+])
+def test_blocksparse_plan_equals_in_kernel_merge(sides, D, B, H, radius, sink):
+    """The host-built plan (merged unit lists, heaviest squares first) gives the
+    same output, bit for bit, as the kernel's own per-CTA merge."""
+    step = len(sides) - 1
+    L, N = cache_len(sides, step), sides[step] ** 2
+    q = randn_bf16((B, H, N, D), 41)
+    k = randn_bf16((B, H, L, D), 42)
+    v = randn_bf16((B, H, L, D), 43)
+    p = V.problem(B, H, D, sides)
+    rp, ent, sink_len = V.var_block_mask_build(p, step, 8, radius, sink)
+    plan = [torch.as_tensor(a, device=DEV) for a in V.var_block_mask_plan(p, step, 8, rp, ent, sink_len)]
+    rp_d, ent_d = torch.as_tensor(rp, device=DEV), torch.as_tensor(ent, device=DEV)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    o1 = torch.empty_like(qd)
+    o2 = torch.empty_like(qd)
+    V.var_attn_blocksparse(p, step, qd, kd, vd, V.block_mask_struct(8, rp_d, ent_d, sink_len), o1)
+    V.var_attn_blocksparse(p, step, qd, kd, vd, V.block_mask_struct(8, rp_d, ent_d, sink_len, plan), o2)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
+    ref = oracle.attention(q, k, v, L, mask=oracle.mask_spec(sides, step, 8, radius, sink))
+    assert_close(o2, ref, f"planned blocksparse {sides}")
+    check_device_status()
+
+
 def test_blocksparse_covering_window_equals_dense():
     sides, D, B, H = (1, 2, 4, 8, 16, 32), 128, 2, 2
     step, L, N = 5, cache_len(sides, 5), 1024

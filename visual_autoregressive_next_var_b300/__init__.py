@@ -47,7 +47,9 @@ class var_problem(C.Structure):
 
 class var_block_mask(C.Structure):
     _fields_ = [("qblock_side", C.c_int32), ("n_qblocks", C.c_int32), ("sink_len", C.c_int32),
-                ("nnz", C.c_int32), ("row_ptr", C.c_void_p), ("entries", C.c_void_p)]
+                ("nnz", C.c_int32), ("row_ptr", C.c_void_p), ("entries", C.c_void_p),
+                ("n_squares", C.c_int32), ("plan_units", C.c_int32), ("sq_ptr", C.c_void_p),
+                ("sq_units", C.c_void_p), ("sq_order", C.c_void_p)]
 
 
 if not os.path.exists(LIB_PATH):
@@ -75,6 +77,8 @@ _SIGS = {
                                           _P]),
     "var_block_mask_build": (C.c_int, [_PROB, C.c_int32, C.c_int32, C.c_int32, C.c_int32, _P, _P,
                                        C.c_int32, _P, _P, _P]),
+    "var_block_mask_plan": (C.c_int, [_PROB, C.c_int32, C.c_int32, _P, _P, C.c_int32, _P, _P, C.c_int32, _P,
+                                      _P, _P]),
     "var_attn_blocksparse": (C.c_int, [_PROB, C.c_int32, _P, _P, _P,
                                        C.POINTER(var_block_mask), _P, _P]),
     "var_keep_count": (C.c_int32, [C.c_int32, C.c_int32, C.c_int32]),
@@ -245,9 +249,30 @@ def var_block_mask_build(p: var_problem, step: int, qblock_side: int, radius: in
     return row_ptr, entries[: nnz.value], sink.value
 
 
+def var_block_mask_plan(p: var_problem, step: int, qblock_side: int, row_ptr: np.ndarray, entries: np.ndarray,
+                        sink_len: int) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """Host call: the block-sparse kernel's plan, (sq_ptr, sq_units, sq_order) int32 arrays."""
+    rp = np.ascontiguousarray(row_ptr, dtype=np.int32)
+    en = np.ascontiguousarray(entries, dtype=np.int32)
+    n_sq, n_u = C.c_int32(), C.c_int32()
+    _check("var_block_mask_plan",
+           _lib.var_block_mask_plan(C.byref(p), step, qblock_side, rp.ctypes.data, en.ctypes.data, sink_len, None,
+                                    None, 0, None, C.byref(n_sq), C.byref(n_u)))
+    sq_ptr = np.zeros(n_sq.value + 1, dtype=np.int32)
+    sq_units = np.zeros(2 * max(n_u.value, 1), dtype=np.int32)
+    sq_order = np.zeros(n_sq.value, dtype=np.int32)
+    _check("var_block_mask_plan",
+           _lib.var_block_mask_plan(C.byref(p), step, qblock_side, rp.ctypes.data, en.ctypes.data, sink_len,
+                                    sq_ptr.ctypes.data, sq_units.ctypes.data, n_u.value, sq_order.ctypes.data,
+                                    C.byref(n_sq), C.byref(n_u)))
+    return sq_ptr, sq_units[: 2 * n_u.value], sq_order
+
+
 def block_mask_struct(qblock_side: int, row_ptr: torch.Tensor, entries: torch.Tensor,
-                      sink_len: int) -> var_block_mask:
-    """var_block_mask over device copies of var_block_mask_build's arrays."""
+                      sink_len: int, plan: Optional[Tuple[torch.Tensor, torch.Tensor, torch.Tensor]] = None
+                      ) -> var_block_mask:
+    """var_block_mask over device copies of var_block_mask_build's arrays and,
+    optionally, of var_block_mask_plan's (sq_ptr, sq_units, sq_order)."""
     m = var_block_mask()
     m.qblock_side = qblock_side
     m.n_qblocks = row_ptr.numel() - 1
@@ -255,6 +280,13 @@ def block_mask_struct(qblock_side: int, row_ptr: torch.Tensor, entries: torch.Te
     m.nnz = entries.numel()
     m.row_ptr = row_ptr.data_ptr()
     m.entries = entries.data_ptr()
+    if plan is not None:
+        sq_ptr, sq_units, sq_order = plan
+        m.n_squares = sq_order.numel()
+        m.plan_units = sq_units.numel() // 2
+        m.sq_ptr = sq_ptr.data_ptr()
+        m.sq_units = sq_units.data_ptr()
+        m.sq_order = sq_order.data_ptr()
     return m
 
 

@@ -1,7 +1,9 @@
 // The C ABI of include/varattn.h: argument checks, geometry, dispatch.
 #include <cmath>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include "internal.h"
@@ -304,6 +306,83 @@ int var_block_mask_build(const var_problem* p, int32_t step, int32_t qblock_side
     if (nnz_out) *nnz_out = static_cast<int32_t>(nnz);
     if (n_qblocks_out) *n_qblocks_out = n_qb;
     if (sink_len_out) *sink_len_out = sink_len;
+    return VAR_OK;
+}
+
+int var_block_mask_plan(const var_problem* p, int32_t step, int32_t qblock_side, const int32_t* row_ptr,
+                        const int32_t* entries, int32_t sink_len, int32_t* sq_ptr, int32_t* sq_units,
+                        int32_t units_cap, int32_t* sq_order, int32_t* n_squares_out, int32_t* n_units_out)
+{
+    StepGeom g;
+    if (int rc = resolve(p, step, &g)) return rc;
+    if (qblock_side != 8) return VAR_ERR_UNSUPPORTED;
+    if (!row_ptr || !entries || sink_len < 0 || sink_len > g.L) return VAR_ERR_INVALID_ARG;
+    if (g.side % 8 != 0) return VAR_ERR_UNSUPPORTED;
+    const int nb = g.side / 8, nsq = (nb + 1) / 2, n_sq = nsq * nsq;
+    const int n_sink = (sink_len + 63) / 64;
+    std::vector<int32_t> counts(n_sq);
+    long long total = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+        total = 0;
+        for (int sq = 0; sq < n_sq; ++sq) {
+            const int by0 = 2 * (sq / nsq), bx0 = 2 * (sq % nsq);
+            // the union of the (up to) four blocks' sorted lists with membership bits
+            std::vector<std::pair<int32_t, uint32_t>> uni;
+            for (int t = 0; t < 4; ++t) {
+                const int by = by0 + (t >> 1), bx = bx0 + (t & 1);
+                if (by >= nb || bx >= nb) continue;
+                const int qb = by * nb + bx;
+                if (row_ptr[qb] < 0 || row_ptr[qb + 1] < row_ptr[qb]) return VAR_ERR_INVALID_ARG;
+                for (int i = row_ptr[qb]; i < row_ptr[qb + 1]; ++i) {
+                    const int32_t e = entries[i];
+                    const int sc = e >> 24, u = (e >> 12) & 0xFFF, v = e & 0xFFF;
+                    if (e < 0 || sc > step || u >= (p->side[sc] + 7) / 8 || v >= (p->side[sc] + 7) / 8)
+                        return VAR_ERR_INVALID_ARG;
+                    uni.emplace_back(e, 1u << t);
+                }
+            }
+            std::sort(uni.begin(), uni.end());
+            std::vector<std::pair<int32_t, uint32_t>> merged;
+            for (const auto& x : uni) {
+                if (!merged.empty() && merged.back().first == x.first) merged.back().second |= x.second;
+                else merged.push_back(x);
+            }
+            const int cnt = n_sink + static_cast<int>(merged.size());
+            if (cnt > SPARSE_MAX_UNITS) return VAR_ERR_UNSUPPORTED;
+            if (pass == 1) {
+                if (sq_ptr) sq_ptr[sq] = static_cast<int32_t>(total);
+                int32_t* out = sq_units + 2 * total;
+                for (int c = 0; c < n_sink; ++c) {
+                    const uint32_t n = static_cast<uint32_t>(std::min(64, sink_len - 64 * c));
+                    out[2 * c] = -1 - c;
+                    out[2 * c + 1] = static_cast<int32_t>(0xFu | META_SINK | (n == 64 ? META_FULL : 0u) | (n << 16));
+                }
+                for (size_t m = 0; m < merged.size(); ++m) {
+                    const int32_t e = merged[m].first;
+                    const int s = p->side[e >> 24], u = (e >> 12) & 0xFFF, v = e & 0xFFF;
+                    const uint32_t rows = static_cast<uint32_t>(std::min(8, s - 8 * u));
+                    const uint32_t cols = static_cast<uint32_t>(std::min(8, s - 8 * v));
+                    out[2 * (n_sink + m)] = e;
+                    out[2 * (n_sink + m) + 1] = static_cast<int32_t>(merged[m].second | (rows << 8) | (cols << 12) |
+                                                                     ((rows == 8 && cols == 8) ? META_FULL : 0u));
+                }
+            }
+            counts[sq] = cnt;
+            total += cnt;
+        }
+        if (pass == 0) {
+            if (n_squares_out) *n_squares_out = n_sq;
+            if (n_units_out) *n_units_out = static_cast<int32_t>(total);
+            if (!sq_units) return VAR_OK;
+            if (total > units_cap || !sq_ptr || !sq_order) return VAR_ERR_INVALID_ARG;
+        }
+    }
+    sq_ptr[n_sq] = static_cast<int32_t>(total);
+    // squares with more units first (ties: lower index), so the longest CTAs start earliest
+    std::vector<int32_t> order(n_sq);
+    for (int i = 0; i < n_sq; ++i) order[i] = i;
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return counts[a] > counts[b]; });
+    for (int i = 0; i < n_sq; ++i) sq_order[i] = order[i];
     return VAR_OK;
 }
 

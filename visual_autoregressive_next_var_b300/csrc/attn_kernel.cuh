@@ -77,7 +77,7 @@ struct AttnLayout {
     static constexpr int NBAR = B_DR + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // tmem slot, abort flag, unit count
     static constexpr int OFF_U = OFF_MISC + 16;           // block-sparse unit list
-    static constexpr int MAXU = 1024;                     // units per block-sparse CTA
+    static constexpr int MAXU = SPARSE_MAX_UNITS;         // units per block-sparse CTA
     static constexpr int MAXL = 512;                      // entries per query-block list
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;              // + alignment slack
     static constexpr int SMEM_BYTES_SPARSE = OFF_U + MAXU * 8 + 1024;
@@ -128,14 +128,14 @@ struct AttnArgs {
     uint32_t map_ok;        // bit sc: scale sc has a per-scale tensor map
     const int32_t* row_ptr; // [n_qblocks + 1]
     const int32_t* entries; // packed (scale << 24) | (u << 12) | v
+    const int32_t* sq_ptr;  // optional host-built plan: units of square q
+    const int2* sq_units;
+    const int32_t* sq_order;// squares in the order CTAs take them (all heads of one square together)
+    int32_t n_bh;           // B * H
+    int32_t plan_units;     // entries of sq_units
     int32_t sides[VAR_MAX_SCALES];
 };
 
-// unit metadata: bits 0-3 query blocks that keep the unit, bit 4 sink chunk,
-// bit 5 every key valid, bits 8-11 valid key rows, 12-15 valid key columns,
-// 16-22 valid keys of a sink chunk
-constexpr uint32_t META_SINK = 1u << 4;
-constexpr uint32_t META_FULL = 1u << 5;
 
 __device__ __forceinline__ void record_fault(volatile int* abort_flag, int32_t* status, int code)
 {
@@ -313,8 +313,15 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
     bool split = false;        // one query tile; group g takes key tiles j = g (mod 2)
     if constexpr (SPARSE) {
         const int nsq2 = args.nsq * args.nsq;
-        bh = blockIdx.x / nsq2;
-        const int sq = blockIdx.x - bh * nsq2;
+        int sq;
+        if (args.sq_order) {              // planned: square-major, heaviest squares first
+            const int rnk = blockIdx.x / args.n_bh;
+            bh = blockIdx.x - rnk * args.n_bh;
+            sq = min(max(__ldg(args.sq_order + rnk), 0), nsq2 - 1);
+        } else {
+            bh = blockIdx.x / nsq2;
+            sq = blockIdx.x - bh * nsq2;
+        }
         by0 = 2 * (sq / args.nsq);
         bx0 = 2 * (sq % args.nsq);
     } else {
@@ -377,7 +384,19 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
     int n_kv = args.n_kv;
     int n_units = 0;
     if constexpr (SPARSE) {
-        n_units = build_units<D>(smem, args, by0, bx0);
+        if (args.sq_units) {
+            // the host-built plan: copy this square's units
+            const int sq = (by0 >> 1) * args.nsq + (bx0 >> 1);
+            const int u0 = min(max(__ldg(args.sq_ptr + sq), 0), args.plan_units);
+            const int u1 = min(max(__ldg(args.sq_ptr + sq + 1), u0), args.plan_units);
+            n_units = min(max(u1 - u0, 0), Lay::MAXU);
+            if (threadIdx.x == 0 && u1 - u0 > Lay::MAXU) atomicCAS(args.status, 0, VAR_ERR_UNSUPPORTED);
+            int2* Uw = reinterpret_cast<int2*>(smem + Lay::OFF_U);
+            for (int i = threadIdx.x; i < n_units; i += blockDim.x) Uw[i] = __ldg(args.sq_units + u0 + i);
+            __syncthreads();
+        } else {
+            n_units = build_units<D>(smem, args, by0, bx0);
+        }
         n_kv = (n_units + 1) >> 1;
     }
 

@@ -92,6 +92,16 @@ static int launch_sparse(const StepGeom& g, const int32_t* sides, int step, cons
     a.row_ptr = mask->row_ptr;
     a.entries = mask->entries;
     for (int i = 0; i <= step; ++i) a.sides[i] = sides[i];
+    a.n_bh = static_cast<int32_t>(BH);
+    if (mask->n_squares > 0) {
+        if (mask->n_squares != a.nsq * a.nsq || !mask->sq_ptr || !mask->sq_units || !mask->sq_order ||
+            mask->plan_units < 0)
+            return VAR_ERR_INVALID_ARG;
+        a.sq_ptr = mask->sq_ptr;
+        a.sq_units = reinterpret_cast<const int2*>(mask->sq_units);
+        a.sq_order = mask->sq_order;
+        a.plan_units = mask->plan_units;
+    }
     const uint64_t ctas = BH * static_cast<uint64_t>(a.nsq) * a.nsq;
     if (ctas > 0x7fffffffull) return VAR_ERR_UNSUPPORTED;
     kern<<<static_cast<unsigned>(ctas), 384, Lay::SMEM_BYTES_SPARSE, st>>>(maps, a);

@@ -11,6 +11,14 @@
 
 namespace varattn {
 
+// Block-sparse unit metadata (the kernel's unit list and the host plan share
+// it): bits 0-3 the square's query blocks that keep the unit, bit 4 a sink
+// chunk, bit 5 every key valid, bits 8-11 valid key rows, 12-15 valid key
+// columns, 16-22 valid keys of a sink chunk.
+constexpr uint32_t META_SINK = 1u << 4;
+constexpr uint32_t META_FULL = 1u << 5;
+constexpr int SPARSE_MAX_UNITS = 1024;   // units per square
+
 // Resolved problem geometry for one step.
 struct StepGeom {
     int B, H, D;
