@@ -150,6 +150,31 @@ def test_fused_pruned_step_equals_chain(fill_first):
     check_device_status()
 
 
+def test_fused_pruned_step_head_dim_64_ragged():
+    """head_dim 64, a 23x23 grid (ragged tiles), random kept set; fused == chain."""
+    sides, D, B, H = (1, 2, 4, 6, 9, 14, 20, 23), 64, 2, 3
+    step = len(sides) - 1
+    L, N = cache_len(sides, step), sides[step] ** 2
+    q = randn_bf16((B, H, N, D), 91).to(DEV)
+    k = randn_bf16((B, H, L, D), 92).to(DEV)
+    v = randn_bf16((B, H, L, D), 93).to(DEV)
+    prev = randn_bf16((B, H, 20 * 20, D), 94).to(DEV)
+    K = 101
+    g = torch.Generator().manual_seed(95)
+    idx = torch.stack([torch.sort(torch.randperm(N, generator=g)[:K])[0] for _ in range(B)]).to(torch.int32).to(DEV)
+    p = V.problem(B, H, D, sides)
+    oc = torch.empty((B, H, K, D), dtype=torch.bfloat16, device=DEV)
+    chain = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=DEV)
+    V.var_attn_pruned(p, step, q, k, v, idx, K, oc)
+    V.var_restore_scatter(p, step, prev, oc, idx, K, chain)
+    fused = torch.full((B, H, N, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    V.var_attn_pruned_scatter(p, step, q, k, v, idx, K, fused)
+    V.var_restore_fill(p, step, prev, idx, K, fused)
+    torch.cuda.synchronize()
+    assert torch.equal(fused, chain)
+    check_device_status()
+
+
 # ---------------------------------------------------------------- pruned attention
 
 @pytest.mark.parametrize("K", [1, 130, 819, 4096])
