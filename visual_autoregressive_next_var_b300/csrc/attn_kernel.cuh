@@ -511,7 +511,6 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
                     tc_fence_after();
                     qk(g0, g0 % NS, 0);
                     umma_commit(bar(Lay::B_SF + g0));
-                    umma_commit(bar(Lay::B_KE + g0 % NS));
                 }
                 for (int j = 0; ok && j < n_kv; ++j) {
                     const int g1 = j & 1, jj = j >> 1;
@@ -521,14 +520,12 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
                         break;
                     tc_fence_after();
                     pv(g1, s, jj > 0);
-                    umma_commit(bar(Lay::B_VE + s));
                     const int jn = j + 2;
                     if (jn < n_kv) {
                         if (!(ok = mbar_wait(bar(Lay::B_KF + jn % NS), (jn / NS) & 1, abort_flag))) break;
                         tc_fence_after();
                         qk(g1, jn % NS, 0);
                         umma_commit(bar(Lay::B_SF + g1));
-                        umma_commit(bar(Lay::B_KE + jn % NS));
                     }
                 }
             } else {
@@ -540,7 +537,6 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
                         umma_commit(bar(Lay::B_SF + 0));
                         qk(1, 0, 1);
                         umma_commit(bar(Lay::B_SF + 1));
-                        umma_commit(bar(Lay::B_KE + 0));
                     }
                 }
                 for (int j = 0; ok && j < n_kv; ++j) {
@@ -563,11 +559,9 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
                     if (!(ok = mbar_wait(bar(Lay::B_PF + 1), j & 1, abort_flag))) break;
                     tc_fence_after();
                     pv(1, s, j > 0);
-                    umma_commit(bar(Lay::B_VE + s));
                     if (more) {
                         qk(1, s1, 1);
                         umma_commit(bar(Lay::B_SF + 1));
-                        umma_commit(bar(Lay::B_KE + s1));
                     }
                 }
             }
@@ -623,11 +617,21 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
         const int n_local = split ? (n_kv + 1 - g) / 2 : n_kv;
         for (int jj = 0; jj < n_local; ++jj) {
             const int j = split ? 2 * jj + g : jj;
-            if (!mbar_wait(bar(Lay::B_SF + g), jj & 1, abort_flag)) {
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(Lay::B_SF + g), jj & 1, abort_flag))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            // Ring slots this S proves free, released here rather than by tensor-core
+            // commits (each commit costs the pipe time): the products that last read
+            // K_j (this step's QK of both tiles) and the V of the step before were
+            // issued ahead of the QK whose completion this wait observed, and the
+            // tensor core completes its work in issue order.
+            if (r == 0 && (split || g == 1)) {
+                const int jv = split ? j - 2 : j - 1;
+                mbar_arrive(bar(Lay::B_KE + j % NS));
+                if (jv >= 0) mbar_arrive(bar(Lay::B_VE + jv % NS));
+            }
             uint32_t s[4][32];
 #pragma unroll
             for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
