@@ -71,8 +71,8 @@ struct AttnLayout {
     static constexpr int B_VF = B_KE + NS;       // [NS] V slot full
     static constexpr int B_VE = B_VF + NS;       // [NS] V slot free
     static constexpr int B_SF = B_VE + NS;       // [2]  S_t computed
-    static constexpr int B_PF = B_SF + 2;        // [2]  P_t written (and O_t rescaled)
-    static constexpr int B_OF = B_PF + 2;        // [1]  all products done
+    static constexpr int B_PF = B_SF + 2;        // [4]  P_t written up to half h, at 2t + h (O_t rescaled first)
+    static constexpr int B_OF = B_PF + 4;        // [1]  all products done
     static constexpr int B_DR = B_OF + 1;        // [1]  drain before teardown
     static constexpr int NBAR = B_DR + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // tmem slot, abort flag, unit count
@@ -297,6 +297,16 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
     constexpr int NS = Lay::NS;
     constexpr bool GATHER = MODE == MODE_GATHER;
     constexpr bool SPARSE = MODE == MODE_SPARSE;
+    // Publish P per 64-key half (the PV of the first half overlaps the second
+    // half's exponentials).  Measured: faster for the block-sparse kernel, a
+    // little slower for the dense and gathered ones, whose PV then waits once.
+    constexpr bool P_HALVES = SPARSE;
+    // Free K/V ring slots from a softmax thread that has seen the next S (no
+    // tensor-core commit in the issue stream) or by commits after the last
+    // product that reads them (the slot frees sooner).  Measured: the first is
+    // faster for the gathered kernel, the second for the dense one, whose
+    // two-slot ring then feeds the next value tile sooner.
+    constexpr bool SOFT_RELEASE = GATHER;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -352,10 +362,8 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
             mbar_init(bar(Lay::B_VF + s), 1);
             mbar_init(bar(Lay::B_VE + s), 1);
         }
-        for (int t = 0; t < 2; ++t) {
-            mbar_init(bar(Lay::B_SF + t), 1);
-            mbar_init(bar(Lay::B_PF + t), 128);
-        }
+        for (int t = 0; t < 2; ++t) mbar_init(bar(Lay::B_SF + t), 1);
+        for (int t = 0; t < 4; ++t) mbar_init(bar(Lay::B_PF + t), 128);
         mbar_init(bar(Lay::B_OF), 1);
         mbar_init(bar(Lay::B_DR), 1);
         *abort_flag = 0;
@@ -492,14 +500,26 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
                             IDESC_QK, kk > 0 ? 1u : 0u);
                 }
             };
-            auto pv = [&](int t, int s, bool acc) {
+            // O_t += P_t V_s.  With P_HALVES each 64-key half is issued as soon as
+            // the softmax has written that half of P; otherwise once all of P is
+            // written (the wait on phase `ph` of the barrier)
+            auto pv = [&](int t, int s, bool acc, uint32_t ph) -> bool {
                 const uint32_t vb = sbase + Lay::OFF_V + s * Lay::TILE_BYTES;
                 const uint32_t dst = tmem + (t ? Lay::COL_O1 : Lay::COL_O0);
                 const uint32_t pa = tmem + (t ? Lay::COL_S1 : Lay::COL_S0);
+                for (int h = 0; h < 2; ++h) {
+                    if (P_HALVES || h == 0) {   // without halves: one wait, for all of P
+                        if (!mbar_wait(bar(Lay::B_PF + 2 * t + (P_HALVES ? h : 1)), ph, abort_flag)) return false;
+                        tc_fence_after();
+                    }
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    umma_ts(dst, pa + kk * 8, sdesc_sw128(vb + kk * 2048, Lay::HALF_BYTES, 1024),
-                            IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        const int kk = 4 * h + k4;
+                        umma_ts(dst, pa + kk * 8, sdesc_sw128(vb + kk * 2048, Lay::HALF_BYTES, 1024),
+                                IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+                    }
+                }
+                return true;
             };
             bool ok = mbar_wait(bar(Lay::B_QF + 0), 0, abort_flag) &&
                       (split || mbar_wait(bar(Lay::B_QF + 1), 0, abort_flag));
@@ -511,21 +531,22 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
                     tc_fence_after();
                     qk(g0, g0 % NS, 0);
                     umma_commit(bar(Lay::B_SF + g0));
+                    if (!SOFT_RELEASE) umma_commit(bar(Lay::B_KE + g0 % NS));
                 }
                 for (int j = 0; ok && j < n_kv; ++j) {
                     const int g1 = j & 1, jj = j >> 1;
                     const int s = j % NS;
                     if (!(ok = mbar_wait(bar(Lay::B_VF + s), (j / NS) & 1, abort_flag) &&
-                               mbar_wait(bar(Lay::B_PF + g1), jj & 1, abort_flag)))
+                               pv(g1, s, jj > 0, jj & 1)))
                         break;
-                    tc_fence_after();
-                    pv(g1, s, jj > 0);
+                    if (!SOFT_RELEASE) umma_commit(bar(Lay::B_VE + s));
                     const int jn = j + 2;
                     if (jn < n_kv) {
                         if (!(ok = mbar_wait(bar(Lay::B_KF + jn % NS), (jn / NS) & 1, abort_flag))) break;
                         tc_fence_after();
                         qk(g1, jn % NS, 0);
                         umma_commit(bar(Lay::B_SF + g1));
+                        if (!SOFT_RELEASE) umma_commit(bar(Lay::B_KE + jn % NS));
                     }
                 }
             } else {
@@ -537,6 +558,7 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
                         umma_commit(bar(Lay::B_SF + 0));
                         qk(1, 0, 1);
                         umma_commit(bar(Lay::B_SF + 1));
+                        if (!SOFT_RELEASE) umma_commit(bar(Lay::B_KE + 0));
                     }
                 }
                 for (int j = 0; ok && j < n_kv; ++j) {
@@ -545,23 +567,20 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
                     const bool more = j + 1 < n_kv;
                     const int s1 = (j + 1) % NS;
                     const uint32_t ph1 = ((j + 1) / NS) & 1;
-                    ok = mbar_wait(bar(Lay::B_VF + s), ph, abort_flag) &&
-                         mbar_wait(bar(Lay::B_PF + 0), j & 1, abort_flag);
+                    ok = mbar_wait(bar(Lay::B_VF + s), ph, abort_flag) && pv(0, s, j > 0, j & 1);
                     if (!ok) break;
-                    tc_fence_after();
-                    pv(0, s, j > 0);
                     if (more) {
                         if (!(ok = mbar_wait(bar(Lay::B_KF + s1), ph1, abort_flag))) break;
                         tc_fence_after();
                         qk(0, s1, 0);
                         umma_commit(bar(Lay::B_SF + 0));
                     }
-                    if (!(ok = mbar_wait(bar(Lay::B_PF + 1), j & 1, abort_flag))) break;
-                    tc_fence_after();
-                    pv(1, s, j > 0);
+                    if (!(ok = pv(1, s, j > 0, j & 1))) break;
+                    if (!SOFT_RELEASE) umma_commit(bar(Lay::B_VE + s));
                     if (more) {
                         qk(1, s1, 1);
                         umma_commit(bar(Lay::B_SF + 1));
+                        if (!SOFT_RELEASE) umma_commit(bar(Lay::B_KE + s1));
                     }
                 }
             }
@@ -622,12 +641,11 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
                 break;
             }
             tc_fence_after();
-            // Ring slots this S proves free, released here rather than by tensor-core
-            // commits (each commit costs the pipe time): the products that last read
-            // K_j (this step's QK of both tiles) and the V of the step before were
-            // issued ahead of the QK whose completion this wait observed, and the
-            // tensor core completes its work in issue order.
-            if (r == 0 && (split || g == 1)) {
+            // SOFT_RELEASE: ring slots this S proves free.  The products that last
+            // read K_j (this step's QK of both tiles) and the V of the step before
+            // were issued ahead of the QK whose completion this wait observed, and
+            // the tensor core completes its work in issue order.
+            if (SOFT_RELEASE && r == 0 && (split || g == 1)) {
                 const int jv = split ? j - 2 : j - 1;
                 mbar_arrive(bar(Lay::B_KE + j % NS));
                 if (jv >= 0) mbar_arrive(bar(Lay::B_VE + jv % NS));
@@ -691,7 +709,9 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
             const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
             l_run *= alpha;
             m_run = m_new;
-            // P = exp2(S * scale*log2e - m), packed to bf16 pairs, 16 columns at a time
+            // P = exp2(S * scale*log2e - m), packed to bf16 pairs, 16 columns at a
+            // time; each 64-key half is published as soon as it is written, so the
+            // PV of the first half overlaps the exponentials of the second
             const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
             const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(neg_m, neg_m);
             uint64_t sum2 = f2_pack(0.f, 0.f);
@@ -709,28 +729,32 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
                     pk[c] = pack_bf16x2(p0, p1);
                 }
                 tmem_st16(tS + cc * 16, pk);
+                if (cc == 1 && __any_sync(0xffffffffu, need && jj > 0)) {
+                    // O_t *= alpha where the running maximum moved, before the first half
+                    // of this step's P is published (every earlier PV of this tile has
+                    // completed: it was issued ahead of the QK whose S this thread
+                    // waited for)
+#pragma unroll
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c0, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                        tmem_st32(tO + c0, o);
+                    }
+                }
+                if (cc == 3 || (P_HALVES && cc == 1)) {
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(bar(Lay::B_PF + 2 * g + (cc >> 1)));
+                }
             }
             {
                 float a0, a1;
                 f2_unpack(sum2, a0, a1);
                 l_run += a0 + a1;
             }
-            // O_t *= alpha where the running maximum moved (the previous PV has
-            // completed: its commit preceded this tile's S commit)
-            if (__any_sync(0xffffffffu, need && jj > 0)) {
-#pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + c0, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                    tmem_st32(tO + c0, o);
-                }
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar(Lay::B_PF + g));
         }
         if (ok) ok = mbar_wait(bar(Lay::B_OF), 0, abort_flag);
         // split CTA: group 1 hands its row's (m, l) to group 0, which merges
