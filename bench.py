@@ -561,39 +561,86 @@ def run_gpu(args):
                 "traffic": ncu_traffic(f"{kernel_names[dom_name]}:final_step_1024px"),
                 "algorithmic_bytes_per_launch": row_bytes[dom_name], "launch_ms": per_row[dom]}
 
-    # end to end through the public API with host buffers
+    # end to end through the public API with host buffers: every step uploads its
+    # inputs (Q, the whole K/V cache, X, the previous step's output) from pinned
+    # host memory and downloads its results.  Pipelined over two device buffer
+    # sets and three streams, as a run of steps would be: step i+1's upload and
+    # step i-1's download overlap step i's kernels.  The serial order (upload,
+    # kernels, download, one stream) is reported beside it.
     host = {"q": inp.q[FINAL].pin_memory(), "k": inp.k.pin_memory(), "v": inp.v.pin_memory(),
             "x": inp.x[FINAL].pin_memory(), "prev": step.prev.cpu().pin_memory()}
-    outs = {"o_dense": torch.empty(step.o_dense.shape, dtype=torch.bfloat16).pin_memory(),
-            "idx": torch.empty(step.idx.shape, dtype=torch.int32).pin_memory(),
-            "o_pruned": torch.empty(step.o_pruned.shape, dtype=torch.bfloat16).pin_memory(),
-            "o_sparse": torch.empty(step.o_sparse.shape, dtype=torch.bfloat16).pin_memory()}
+    outs = [{"o_dense": torch.empty(step.o_dense.shape, dtype=torch.bfloat16).pin_memory(),
+             "idx": torch.empty(step.idx.shape, dtype=torch.int32).pin_memory(),
+             "o_pruned": torch.empty(step.o_pruned.shape, dtype=torch.bfloat16).pin_memory(),
+             "o_sparse": torch.empty(step.o_sparse.shape, dtype=torch.bfloat16).pin_memory()} for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = sum(t.numel() * t.element_size() for t in outs.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs[0].values())
+    sets = [step, Step(V, dev, inp)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_fn():
-        step.q.copy_(host["q"], non_blocking=True)
-        step.k.copy_(host["k"], non_blocking=True)
-        step.v.copy_(host["v"], non_blocking=True)
-        step.x.copy_(host["x"], non_blocking=True)
-        step.prev.copy_(host["prev"], non_blocking=True)
+    def upload(st, strm):
+        with torch.cuda.stream(strm):
+            st.q.copy_(host["q"], non_blocking=True)
+            st.k.copy_(host["k"], non_blocking=True)
+            st.v.copy_(host["v"], non_blocking=True)
+            st.x.copy_(host["x"], non_blocking=True)
+            st.prev.copy_(host["prev"], non_blocking=True)
+
+    def download(st, o, strm):
+        with torch.cuda.stream(strm):
+            o["o_dense"].copy_(st.o_dense, non_blocking=True)
+            o["idx"].copy_(st.idx, non_blocking=True)
+            o["o_pruned"].copy_(st.o_pruned, non_blocking=True)
+            o["o_sparse"].copy_(st.o_sparse, non_blocking=True)
+
+    def e2e_serial():
+        upload(step, stream)
         step.run(stream)
-        outs["o_dense"].copy_(step.o_dense, non_blocking=True)
-        outs["idx"].copy_(step.idx, non_blocking=True)
-        outs["o_pruned"].copy_(step.o_pruned, non_blocking=True)
-        outs["o_sparse"].copy_(step.o_sparse, non_blocking=True)
+        download(step, outs[0], stream)
 
+    def e2e_pipelined(n):
+        for i in range(n):
+            b = i & 1
+            st = sets[b]
+            if i >= 2:
+                s_in.wait_event(ev_comp[b])          # step i-2 has finished reading this set
+            upload(st, s_in)
+            ev_in[b].record(s_in)
+            stream.wait_event(ev_in[b])
+            if i >= 2:
+                stream.wait_event(ev_out[b])         # step i-2's results are downloaded
+            st.run(stream)
+            ev_comp[b].record(stream)
+            s_out.wait_event(ev_comp[b])
+            download(st, outs[b], s_out)
+            ev_out[b].record(s_out)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
+
+    e2e_steps = max(4, min(args.steps, 10))
     for _ in range(2):
-        e2e_fn()
-    e2e_steps = max(3, min(args.steps, 10))
+        e2e_serial()
+    e2e_pipelined(2)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
-        e2e_fn()
+        e2e_serial()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_serial = reduce_max(e0.elapsed_time(e1) / e2e_steps, ws, dev)
+    s_in.wait_stream(stream)
+    s_out.wait_stream(stream)
+    e0.record(stream)
+    s_in.wait_stream(stream)                         # the uploads start after e0
+    e2e_pipelined(e2e_steps)
     e1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = reduce_max(e0.elapsed_time(e1) / e2e_steps, ws, dev)
+    del sets[1]
 
     cfg = step_config(inp)
     cfg["l2"] = "inputs larger than L2 (Q/K/V 206 MB + X 34 MB per step)"
@@ -607,7 +654,10 @@ def run_gpu(args):
                       f"{flops_exec / 1e9:.1f} GFLOP -> {ws * flops_exec / ms_max / 1e9:.1f} TFLOP/s",
         "roofline": roof,
         "e2e": {"value": ws * flops_equiv / ms_e2e / 1e9, "unit": "TFLOP/s", "ms_per_step": ms_e2e,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "mode": f"pipelined over {e2e_steps} steps: upload of step i+1 and download of step i-1 "
+                        "overlap step i's kernels (two device buffer sets, three streams)",
+                "serial_ms_per_step": ms_serial},
         "gpu_launches": args.steps * LAUNCHES_PER_STEP,
         "clocks": clk.summary(),
         "rows": rows,
