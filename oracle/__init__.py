@@ -59,11 +59,15 @@ def lib():
                                            C.c_double, P, P, P]
         L.oracle_saliency.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
                                       C.c_double, P, P, P]
+        L.oracle_unit_mass.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
+                                        C.c_double, P, P, P, C.c_int, P]
+        L.oracle_attention_keep.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
+                                            C.c_double, P, P, P, P, P]
         L.oracle_num_threads.restype = C.c_int
         L.oracle_num_threads.argtypes = []
         for f in ("oracle_attention", "oracle_block_mask_rows", "oracle_pivot_mean",
                   "oracle_pivot_scores", "oracle_pivot_select", "oracle_restore_scatter",
-                  "oracle_attention_lse", "oracle_saliency"):
+                  "oracle_attention_lse", "oracle_saliency", "oracle_unit_mass", "oracle_attention_keep"):
             getattr(L, f).restype = C.c_int
         _lib = L
     return _lib
@@ -189,6 +193,163 @@ def branch_halved_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, L
     h = B // 2
     cond = attention(q[:h].contiguous(), k[:h].contiguous(), v[:h].contiguous(), L, scale=scale)
     return np.concatenate([cond, cond], axis=0)
+
+
+# ----------------------------------------------------------------------------- dynamic pattern
+# SparVAR (abstract): the sparse attention pattern of later high-resolution
+# scales is predicted from a sparse decision scale and carried to them by index
+# mapping, giving scale self-similar sparse attention.  The pages fix no score,
+# threshold or mapping formula; the reading implemented here:
+#   units     the decision step's keys in 64-key units: the sink range (leading
+#             scales with side <= sink_max_side) in 64-token chunks, then every
+#             8x8 key block of each later scale up to the decision scale;
+#   score     A[qb, u]: the attention mass unit u receives, averaged over the 64
+#             queries of the decision step's 8x8 query block qb, its heads and
+#             batch elements (one pattern, as the block mask is one for all);
+#   select    per qb the sinks, then the other units by score (equal scores:
+#             lower unit first) until the kept mass reaches tau of the total;
+#   map       a target step's query block takes the decision block under its
+#             centre; kept blocks of scales below the decision scale are kept
+#             as they are, kept blocks of the decision scale are kept and also
+#             mapped into every later scale up to the target, to the blocks
+#             that meet the rescaled block (rounded outward).
+
+
+def sparvar_units(sides: Sequence[int], d: int, sink_max_side: int):
+    """The decision step's key units: (unit_of_key int32[L_d], units, n_sink).
+    units[u] = ("sink", c) for tokens [64c, 64c + 64) of the sink range, or
+    (scale, u, v) for key block (u, v) of that scale (rows 8u.., cols 8v..)."""
+    sink_len = 0
+    sc = 0
+    while sc <= d and sides[sc] <= sink_max_side:
+        sink_len += sides[sc] ** 2
+        sc += 1
+    L = sum(sides[i] ** 2 for i in range(d + 1))
+    unit_of = np.zeros(L, dtype=np.int32)
+    units = []
+    for c in range((sink_len + 63) // 64):
+        unit_of[64 * c:min(64 * c + 64, sink_len)] = len(units)
+        units.append(("sink", c))
+    n_sink = len(units)
+    off = sink_len
+    for scale in range(sc, d + 1):
+        s = sides[scale]
+        nbs = (s + 7) // 8
+        for u in range(nbs):
+            for v in range(nbs):
+                for r in range(8 * u, min(8 * u + 8, s)):
+                    unit_of[off + r * s + 8 * v:off + r * s + min(8 * v + 8, s)] = len(units)
+                units.append((scale, u, v))
+        off += s * s
+    return unit_of, units, n_sink
+
+
+def sparvar_scores(q_d: torch.Tensor, k: torch.Tensor, sides: Sequence[int], d: int, sink_max_side: int,
+                   scale: Optional[float] = None) -> np.ndarray:
+    """A[qb, u] fp64: unit u's attention mass averaged over the 64 queries of the
+    decision step's 8x8 query block qb (row-major blocks), heads and batch."""
+    B, H, N, D = q_d.shape
+    s_d = sides[d]
+    assert N == s_d * s_d and s_d % 8 == 0
+    unit_of, units, _ = sparvar_units(sides, d, sink_max_side)
+    L = len(unit_of)
+    U = len(units)
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    mass = np.zeros((B, H, N, U), dtype=np.float64)
+    if lib().oracle_unit_mass(B, H, N, L, k.shape[2], D, scale, _ptr(_bits(q_d)), _ptr(_bits(k)),
+                              _ptr(unit_of), U, _ptr(mass)) != 0:
+        raise ValueError("oracle_unit_mass failed")
+    nb = s_d // 8
+    g = mass.reshape(B, H, nb, 8, nb, 8, U)            # [b, h, by, y, bx, x, u]
+    return g.sum(axis=(0, 1, 3, 5)).reshape(nb * nb, U) / (B * H * 64)
+
+
+def sparvar_select(A: np.ndarray, n_sink: int, tau: float):
+    """Per decision query block: the kept non-sink unit indices (ascending).  The
+    sinks are always kept; the other units are taken by decreasing score (equal
+    scores: lower unit first) until the kept mass reaches tau of the row total.
+    Masses are added in fp64 in that order."""
+    kept = []
+    for row in A:
+        total = 0.0
+        for x in row:
+            total += float(x)
+        have = 0.0
+        for u in range(n_sink):
+            have += float(row[u])
+        order = sorted(range(n_sink, len(row)), key=lambda u: (-float(row[u]), u))
+        take = []
+        for u in order:
+            if have >= tau * total:
+                break
+            take.append(u)
+            have += float(row[u])
+        kept.append(sorted(take))
+    return kept
+
+
+def sparvar_keep_mask(sides: Sequence[int], d: int, k_step: int, units, kept, sink_max_side: int) -> np.ndarray:
+    """Token-level keep mask [N_k, L_k] (uint8) of the target step k >= d, built
+    from the definition: per target query token, its 8x8 block, the decision
+    block under that block's centre, and the keys its kept units cover there."""
+    s_d, s_k = sides[d], sides[k_step]
+    nb_d, nb_k = s_d // 8, s_k // 8
+    offs = np.cumsum([0] + [s * s for s in sides[:k_step + 1]])
+    L = int(offs[-1])
+    sink_len = 0
+    sc = 0
+    while sc <= k_step and sides[sc] <= sink_max_side:
+        sink_len += sides[sc] ** 2
+        sc += 1
+    block_keys = np.zeros((nb_d * nb_d, L), dtype=np.uint8)   # keys kept by each decision block
+    for qb, lst in enumerate(kept):
+        row = block_keys[qb]
+        row[:sink_len] = 1
+        for u_idx in lst:
+            scale, u, v = units[u_idx]
+            targets = [(scale, u, v)] if scale < d else []
+            if scale == d:
+                for sc2 in range(d, k_step + 1):
+                    s2 = sides[sc2]
+                    # rows of the decision block [8u, 8u+8) clipped, rescaled to s2, outward
+                    r0, r1 = 8 * u, min(8 * u + 8, s_d)
+                    c0, c1 = 8 * v, min(8 * v + 8, s_d)
+                    lo_r, hi_r = (r0 * s2) // s_d, -((-r1 * s2) // s_d)
+                    lo_c, hi_c = (c0 * s2) // s_d, -((-c1 * s2) // s_d)
+                    for uu in range((s2 + 7) // 8):
+                        if not (8 * uu < hi_r and lo_r < min(8 * uu + 8, s2)):
+                            continue
+                        for vv in range((s2 + 7) // 8):
+                            if 8 * vv < hi_c and lo_c < min(8 * vv + 8, s2):
+                                targets.append((sc2, uu, vv))
+            for (sc2, uu, vv) in targets:
+                s2 = sides[sc2]
+                for r in range(8 * uu, min(8 * uu + 8, s2)):
+                    a = offs[sc2] + r * s2
+                    row[a + 8 * vv:a + min(8 * vv + 8, s2)] = 1
+    keep = np.zeros((s_k * s_k, L), dtype=np.uint8)
+    for y in range(s_k):
+        for x in range(s_k):
+            by, bx = y // 8, x // 8
+            dy = ((2 * by + 1) * nb_d) // (2 * nb_k)
+            dx = ((2 * bx + 1) * nb_d) // (2 * nb_k)
+            keep[y * s_k + x] = block_keys[dy * nb_d + dx]
+    return keep
+
+
+def attention_keep(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, L: int, keep: np.ndarray,
+                   scale: Optional[float] = None) -> np.ndarray:
+    """Attention of q [B,H,N,D] over the first L keys, query i keeping key j iff
+    keep[i, j] (one mask for every (b, h)); [B, H, N, D] fp64."""
+    B, H, N, D = q.shape
+    keep = np.ascontiguousarray(keep, dtype=np.uint8)
+    assert keep.shape == (N, L)
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    out = np.zeros((B, H, N, D), dtype=np.float64)
+    if lib().oracle_attention_keep(B, H, N, L, k.shape[2], D, scale, _ptr(_bits(q)), _ptr(_bits(k)),
+                                   _ptr(_bits(v)), _ptr(keep), _ptr(out)) != 0:
+        raise ValueError("oracle_attention_keep failed")
+    return out
 
 
 def block_mask_rows(m: MaskSpec, q0: int, q1: int) -> np.ndarray:

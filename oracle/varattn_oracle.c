@@ -24,6 +24,12 @@
  *    describes FastVAR's selection.
  *  - Restore + scatter: ARVAR Key Design 3, Eq. (8)-(9):
  *    Y_T = Scatter(Up(Y_{T-N}; h_T, w_T), I_T, Yhat_T), scatter overwrites.
+ *  - Dynamic sparse pattern: SparVAR abstract -- the sparse attention pattern
+ *    of later high-resolution scales is predicted from a sparse decision
+ *    scale.  This file gives the attention mass each unit of keys receives
+ *    from each decision-step query (oracle_unit_mass) and attention under an
+ *    explicit token-level keep mask (oracle_attention_keep); the selection and
+ *    index mapping built on them are in __init__.py.
  *
  * Readings taken where the pages are silent:
  *  - no causal mask inside a step; softmax scale 1/sqrt(head_dim);
@@ -139,12 +145,12 @@ int oracle_block_mask_rows(const oracle_mask_spec* m, int q0, int q1, uint8_t* o
 /* One output row: o = sum_j softmax_j(q.k_j * scale) v_j over kept keys.
  * sbuf holds L doubles.  An empty key set gives a zero row. */
 static void attend_row(int L, int D, double scale, const uint16_t* q, const uint16_t* K,
-                       const uint16_t* V, const oracle_mask_spec* m, int qi, double* sbuf,
-                       double* out)
+                       const uint16_t* V, const oracle_mask_spec* m, const uint8_t* keep_row, int qi,
+                       double* sbuf, double* out)
 {
     double mx = -INFINITY;
     for (int j = 0; j < L; j++) {
-        if (m && !key_kept(m, qi, j)) { sbuf[j] = -INFINITY; continue; }
+        if ((m && !key_kept(m, qi, j)) || (keep_row && !keep_row[j])) { sbuf[j] = -INFINITY; continue; }
         double dot = 0.0;
         for (int d = 0; d < D; d++) dot += bf16_to_f64(q[d]) * bf16_to_f64(K[(size_t)j * D + d]);
         sbuf[j] = dot * scale;
@@ -194,7 +200,39 @@ int oracle_attention(int B, int H, int N, int L, int kv_cap, int D, double scale
                 const long bh = flat / N;
                 const int qi = (int)(flat % N);
                 attend_row(L, D, scale, q + (size_t)flat * D, k + (size_t)bh * kv_cap * D,
-                           v + (size_t)bh * kv_cap * D, m, qi, sbuf, o + (size_t)r * D);
+                           v + (size_t)bh * kv_cap * D, m, NULL, qi, sbuf, o + (size_t)r * D);
+            }
+            free(sbuf);
+        }
+    }
+    return bad;
+}
+
+/*
+ * As oracle_attention (all rows), with the kept keys given token by token:
+ * query i of every (b, h) attends to key j < L iff keep[i * L + j] != 0.
+ */
+int oracle_attention_keep(int B, int H, int N, int L, int kv_cap, int D, double scale,
+                          const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                          const uint8_t* keep, double* o)
+{
+    if (B <= 0 || H <= 0 || N < 0 || L <= 0 || D <= 0 || kv_cap < L || !keep) return 1;
+    const long total = (long)B * H * N;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double* sbuf = (double*)malloc(sizeof(double) * (size_t)L);
+        if (!sbuf) {
+#pragma omp atomic write
+            bad = 2;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (long r = 0; r < total; r++) {
+                const long bh = r / N;
+                const int qi = (int)(r % N);
+                attend_row(L, D, scale, q + (size_t)r * D, k + (size_t)bh * kv_cap * D,
+                           v + (size_t)bh * kv_cap * D, NULL, keep + (size_t)qi * L, qi, sbuf,
+                           o + (size_t)r * D);
             }
             free(sbuf);
         }
@@ -278,6 +316,46 @@ int oracle_saliency(int B, int H, int N, int L, int kv_cap, int D, double scale,
                     for (int j = 0; j < L; j++) l += exp(s[j] - mx);
                     for (int j = 0; j < N; j++) out[j] += exp(s[L - N + j] - mx) / l;
                 }
+            }
+            free(s);
+        }
+    }
+    return bad;
+}
+
+/* ------------------------------------------------------------------ */
+/* Dynamic sparse pattern (SparVAR: a sparse decision scale)           */
+/* ------------------------------------------------------------------ */
+
+/*
+ * mass[(bh * N + i) * U + u] = the softmax probability (over all L keys) that
+ * query i of (b, h) gives to the keys j of unit u (unit_of[j] == u), summed:
+ * the attention mass a unit of keys receives.  unit_of[j] in [0, U), j < L.
+ */
+int oracle_unit_mass(int B, int H, int N, int L, int kv_cap, int D, double scale,
+                     const uint16_t* q, const uint16_t* k, const int32_t* unit_of, int U,
+                     double* mass)
+{
+    if (B <= 0 || H <= 0 || N <= 0 || L <= 0 || D <= 0 || kv_cap < L || U <= 0 || !unit_of) return 1;
+    for (int j = 0; j < L; j++)
+        if (unit_of[j] < 0 || unit_of[j] >= U) return 1;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)L);
+        if (!s) {
+#pragma omp atomic write
+            bad = 2;
+        } else {
+#pragma omp for schedule(static)
+            for (long r = 0; r < (long)B * H * N; r++) {
+                const long bh = r / N;
+                const double mx = row_scores(L, D, scale, q + (size_t)r * D, k + (size_t)bh * kv_cap * D, s);
+                double l = 0.0;
+                for (int j = 0; j < L; j++) l += exp(s[j] - mx);
+                double* out = mass + (size_t)r * U;
+                for (int u = 0; u < U; u++) out[u] = 0.0;
+                for (int j = 0; j < L; j++) out[unit_of[j]] += exp(s[j] - mx) / l;
             }
             free(s);
         }

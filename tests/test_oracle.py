@@ -360,3 +360,184 @@ def test_restore_rejects_bad_indices():
         oracle.restore_scatter(prev, oc, np.array([[3, 3]], np.int32), 3)   # duplicate
     with pytest.raises(ValueError):
         oracle.restore_scatter(prev, oc, np.array([[0, 9]], np.int32), 3)   # out of range
+
+
+# ---------------------------------------------------------------- dynamic pattern (SparVAR)
+
+SV_SIDES = (1, 2, 4, 8, 16, 24, 32)      # sinks: the 1, 2, 4 scales (21 tokens) at sink_max_side 4
+SV_SINK = 4
+
+
+def _np_probs(q, k, L):
+    D = q.shape[-1]
+    s = np.einsum("bhnd,bhld->bhnl", _np_bits(q), _np_bits(k[:, :, :L])) / np.sqrt(D)
+    P = np.exp(s - s.max(-1, keepdims=True))
+    return P / P.sum(-1, keepdims=True)
+
+
+def test_sparvar_units_partition_the_keys():
+    d = 5                                             # decision scale 24
+    unit_of, units, n_sink = oracle.sparvar_units(SV_SIDES, d, SV_SINK)
+    L = cum(SV_SIDES, d)
+    assert len(unit_of) == L and n_sink == 1
+    sizes = np.bincount(unit_of, minlength=len(units))
+    assert sizes[0] == 21                             # the sink range in one 64-token chunk
+    for idx in range(n_sink, len(units)):
+        sc, u, v = units[idx]
+        s = SV_SIDES[sc]
+        assert sizes[idx] == min(8, s - 8 * u) * min(8, s - 8 * v)
+    assert len(units) == 1 + 1 + 4 + 9               # 8: one block, 16: 2x2, 24: 3x3
+    # a block's keys are exactly its rows and columns of its scale
+    off = cum(SV_SIDES, 4)                            # start of the 24 scale
+    j = off + 9 * 24 + 17                             # row 9, column 17 -> block (1, 2)
+    assert units[unit_of[j]] == (5, 1, 2)
+
+
+def test_sparvar_unit_mass_matches_bruteforce():
+    B, H, D, d = 2, 2, 16, 4                          # decision scale 16 (2 x 2 query blocks)
+    L, N = cum(SV_SIDES, d), 16 * 16
+    q = randn_bf16((B, H, N, D), 701)
+    k = randn_bf16((B, H, L + 5, D), 702)             # a cache with spare capacity
+    unit_of, units, n_sink = oracle.sparvar_units(SV_SIDES, d, SV_SINK)
+    P = _np_probs(q, k, L)
+    mass = np.zeros(P.shape[:3] + (len(units),))
+    for u in range(len(units)):
+        mass[..., u] = P[..., unit_of == u].sum(-1)
+    A_ref = mass.reshape(B, H, 2, 8, 2, 8, len(units)).sum(axis=(0, 1, 3, 5)).reshape(4, -1) / (B * H * 64)
+    A = oracle.sparvar_scores(q, k, SV_SIDES, d, SV_SINK)
+    assert np.max(np.abs(A - A_ref)) < 1e-13
+    assert np.allclose(A.sum(axis=1), 1.0, rtol=0, atol=1e-12)   # every query's mass is 1
+
+
+def test_sparvar_unit_mass_uniform_closed_form():
+    # q = 0: every key gets 1/L, so a unit's mass is its size over L
+    B, H, D, d = 1, 2, 8, 4
+    L = cum(SV_SIDES, d)
+    q = torch.zeros((B, H, 256, D), dtype=torch.bfloat16)
+    k = randn_bf16((B, H, L, D), 703)
+    unit_of, units, _ = oracle.sparvar_units(SV_SIDES, d, SV_SINK)
+    A = oracle.sparvar_scores(q, k, SV_SIDES, d, SV_SINK)
+    sizes = np.bincount(unit_of, minlength=len(units))
+    assert np.allclose(A, np.tile(sizes / L, (4, 1)), rtol=0, atol=1e-14)
+
+
+def test_sparvar_select_threshold_rule():
+    A = np.array([[0.1, 0.3, 0.2, 0.3, 0.1],          # unit 0 is the sink
+                  [0.5, 0.1, 0.1, 0.1, 0.2]])
+    assert oracle.sparvar_select(A, 1, 0.0) == [[], []]
+    assert oracle.sparvar_select(A, 1, 1.0) == [[1, 2, 3, 4], [1, 2, 3, 4]]
+    # tau 0.5: row 0 takes unit 1 (tie with 3, lower index first): 0.1 + 0.3 = 0.4 < 0.5,
+    # then unit 3: 0.7; row 1: the sink alone holds 0.5
+    assert oracle.sparvar_select(A, 1, 0.5) == [[1, 3], []]
+    assert oracle.sparvar_select(A, 1, 0.75) == [[1, 2, 3], [1, 4]]
+    # monotone in tau
+    prev = [set(), set()]
+    for tau in np.linspace(0, 1, 21):
+        cur = [set(x) for x in oracle.sparvar_select(A, 1, tau)]
+        assert all(p <= c for p, c in zip(prev, cur))
+        prev = cur
+
+
+def test_sparvar_keep_mask_identity_at_the_decision_step():
+    d = 5
+    unit_of, units, n_sink = oracle.sparvar_units(SV_SIDES, d, SV_SINK)
+    rng = np.random.default_rng(704)
+    kept = [sorted(rng.choice(np.arange(n_sink, len(units)), size=3, replace=False).tolist()) for _ in range(9)]
+    keep = oracle.sparvar_keep_mask(SV_SIDES, d, d, units, kept, SV_SINK)
+    s = SV_SIDES[d]
+    for i in range(s * s):
+        qb = (i // s // 8) * 3 + (i % s) // 8
+        want = np.isin(unit_of, list(range(n_sink)) + kept[qb]).astype(np.uint8)
+        assert np.array_equal(keep[i], want)
+
+
+def test_sparvar_keep_mask_maps_by_rescaling():
+    # decision 16 (2 x 2 blocks) -> target 32 (4 x 4 blocks): target block (by, bx) reads
+    # decision block (by // 2, bx // 2); a kept 16-scale block (u, v) covers the 24 scale
+    # rows [floor(8u * 1.5), ceil((8u + 8) * 1.5)) and exactly block (u, v) of the 16
+    # scale, and at the 32 scale the 2 x 2 blocks (2u.., 2v..)
+    d, k_step = 4, 6
+    unit_of, units, n_sink = oracle.sparvar_units(SV_SIDES, d, SV_SINK)
+    idx = {units[i]: i for i in range(len(units))}
+    kept = [[idx[(4, 0, 1)], idx[(3, 0, 0)]], [], [], [idx[(4, 1, 1)]]]
+    keep = oracle.sparvar_keep_mask(SV_SIDES, d, k_step, units, kept, SV_SINK)
+    offs = np.cumsum([0] + [s * s for s in SV_SIDES])
+    L = offs[k_step + 1]
+    assert keep.shape == (32 * 32, L)
+
+    def grid(row, sc):
+        s = SV_SIDES[sc]
+        return row[offs[sc]:offs[sc] + s * s].reshape(s, s)
+
+    # a query of target block (0, 1) -> decision block (0, 0): sinks, (3,0,0), (4,0,1) mapped
+    r = keep[0 * 32 + 9]
+    assert r[:21].all()
+    assert grid(r, 3).all()                                   # the whole 8 scale
+    g16 = grid(r, 4)
+    assert g16[:8, 8:].all() and g16.sum() == 64
+    g24 = grid(r, 5)                                          # rows [0, 12) -> blocks 0, 1; cols [12, 24) -> 1, 2
+    want = np.zeros((24, 24), dtype=np.uint8)
+    want[:16, 8:24] = 1
+    assert np.array_equal(g24, want)
+    g32 = grid(r, 6)
+    want = np.zeros((32, 32), dtype=np.uint8)
+    want[:16, 16:32] = 1
+    assert np.array_equal(g32, want)
+    # target block (1, 1) reads decision block (0, 0) too; block (2, 2) reads (1, 1)
+    assert np.array_equal(keep[8 * 32 + 8], keep[0 * 32 + 9])
+    r2 = keep[16 * 32 + 16]
+    assert grid(r2, 3).sum() == 0 and grid(r2, 4)[8:, 8:].all() and grid(r2, 4).sum() == 64
+    # nothing outside the sinks for blocks that kept nothing
+    assert keep[0 * 32 + 20][21:].sum() == 0
+
+
+def test_sparvar_keep_mask_covers_the_rescaled_block():
+    # every key whose position, mapped back to the decision scale, falls inside a kept
+    # decision-scale block is kept; every kept block of a later scale touches it
+    d, k_step = 5, 6                                          # 24 -> 32
+    unit_of, units, n_sink = oracle.sparvar_units(SV_SIDES, d, SV_SINK)
+    kept = [[i for i in range(n_sink, len(units)) if units[i][0] == 5 and (units[i][1] + units[i][2]) % 3 == 0]] * 9
+    keep = oracle.sparvar_keep_mask(SV_SIDES, d, k_step, units, kept, SV_SINK)
+    offs = np.cumsum([0] + [s * s for s in SV_SIDES])
+    row = keep[0]
+    sel = {(units[i][1], units[i][2]) for i in kept[0]}
+    s_d, s2 = 24, 32
+    g = row[offs[6]:offs[6] + s2 * s2].reshape(s2, s2)
+    for y in range(s2):
+        for x in range(s2):
+            # the decision-scale area of this key [y, y+1) x [x, x+1) scaled by 24/32
+            ys = {int(np.floor(y * s_d / s2)), int(np.ceil((y + 1) * s_d / s2)) - 1}
+            xs = {int(np.floor(x * s_d / s2)), int(np.ceil((x + 1) * s_d / s2)) - 1}
+            inside = any((yy // 8, xx // 8) in sel for yy in ys for xx in xs)
+            if inside:
+                assert g[y, x] == 1
+            if g[y, x]:
+                # some decision block of the selection meets this key's whole 8 x 8 block
+                by, bx = y // 8, x // 8
+                ry = range(int(np.floor(8 * by * s_d / s2)), int(np.ceil((8 * by + 8) * s_d / s2)))
+                rx = range(int(np.floor(8 * bx * s_d / s2)), int(np.ceil((8 * bx + 8) * s_d / s2)))
+                assert any((yy // 8, xx // 8) in sel for yy in ry for xx in rx)
+
+
+def test_attention_keep_matches_dense_masked_and_bruteforce():
+    B, H, D = 1, 2, 8
+    sides = (1, 2, 4, 8)
+    L, N = cum(sides, 3), 64
+    q = randn_bf16((B, H, N, D), 705)
+    k = randn_bf16((B, H, L, D), 706)
+    v = randn_bf16((B, H, L, D), 707)
+    ones = np.ones((N, L), dtype=np.uint8)
+    assert np.max(np.abs(oracle.attention_keep(q, k, v, L, ones) - oracle.attention(q, k, v, L))) < 1e-15
+    rng = np.random.default_rng(708)
+    keep = (rng.random((N, L)) < 0.3).astype(np.uint8)
+    keep[5] = 0                                               # a row that keeps nothing: zeros
+    got = oracle.attention_keep(q, k, v, L, keep)
+    s = np.einsum("bhnd,bhld->bhnl", _np_bits(q), _np_bits(k)) / np.sqrt(D)
+    s = np.where(keep[None, None] > 0, s, -np.inf)
+    for i in range(N):
+        if keep[i].sum() == 0:
+            assert np.all(got[:, :, i] == 0)
+            continue
+        p = np.exp(s[:, :, i] - s[:, :, i].max(-1, keepdims=True))
+        ref = np.einsum("bhl,bhld->bhd", p / p.sum(-1, keepdims=True), _np_bits(v))
+        assert np.max(np.abs(got[:, :, i] - ref)) < 1e-12
