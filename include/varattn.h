@@ -326,6 +326,70 @@ VAR_API int var_block_mask_plan(const var_problem* p, int32_t step, int32_t qblo
 VAR_API int var_attn_blocksparse(const var_problem* p, int32_t step, const void* q, const void* k,
                          const void* v, const var_block_mask* mask, void* o, void* stream);
 
+/*
+ * Dynamic sparse pattern ("SparVAR" abstract: the sparse attention pattern of
+ * later high-resolution scales is predicted from a sparse decision scale and
+ * carried to them by an index-mapping mechanism, giving scale self-similar
+ * sparse attention).  The pages fix no formula; this library's reading:
+ *
+ *   units   the decision step's keys in 64-key units: the sink range (the
+ *           leading scales with side <= sink_max_side) in 64-token chunks
+ *           (units [0, n_sink)), then every 8 x 8 key block of each later
+ *           scale up to the decision scale, row-major, scale by scale;
+ *   score   scores[qb][u]: the attention mass unit u receives (softmax over all
+ *           the decision step's keys), averaged over the 64 queries of the
+ *           decision step's 8 x 8 query block qb, the heads and the batch;
+ *   select  per qb: the sinks, then the other units by decreasing score (equal
+ *           scores: lower unit first) until the kept mass reaches tau of the
+ *           row total (masses added in fp64 in that order);
+ *   map     a query block of the target step takes the decision block under its
+ *           centre; its kept blocks of scales below the decision scale are kept
+ *           as they are, its kept blocks of the decision scale are kept and
+ *           mapped into every later scale up to the target, to the blocks that
+ *           meet the block rescaled (rounded outward).
+ *
+ * The result is a block mask in var_block_mask_build's format, for
+ * var_block_mask_plan and var_attn_blocksparse.
+ */
+
+/* HOST: the decision step's unit count U and sink units n_sink.  Errors:
+ * VAR_ERR_UNSUPPORTED (decision side not a multiple of 8 or a sink scale, sink
+ * scales not leading), VAR_ERR_INVALID_ARG (problem). */
+VAR_API int var_sparvar_units(const var_problem* p, int32_t decision_step, int32_t sink_max_side,
+                              int32_t* n_units_out, int32_t* n_sink_units_out);
+
+/* Device workspace bytes var_sparvar_scores needs (0 for an invalid problem). */
+VAR_API size_t var_sparvar_workspace_bytes(const var_problem* p, int32_t decision_step);
+
+/*
+ * Block scores of the decision step on the device: scores [n_qb][U] fp64
+ * (n_qb = (side/8)^2, row-major query blocks; caller-owned device memory).
+ * q: the decision step's queries [B][H][N][D]; k: the cache [B][H][kv_capacity][D].
+ * The mass is computed as attention with the values replaced by each unit's
+ * indicator (head_dim units per pass of the dense attention kernel), then
+ * averaged in a fixed order.  workspace: var_sparvar_workspace_bytes bytes,
+ * 16-byte aligned.  Asynchronous on `stream`.
+ * Errors: as var_attn_dense, VAR_ERR_WORKSPACE (too small), and those of
+ * var_sparvar_units.
+ */
+VAR_API int var_sparvar_scores(const var_problem* p, int32_t decision_step, int32_t sink_max_side,
+                               const void* q, const void* k, void* workspace, size_t workspace_bytes,
+                               double* scores, void* stream);
+
+/*
+ * HOST: the target step's block mask from the decision step's scores (host
+ * copy, [n_qb_d][U] fp64): selection with fraction tau in [0, 1], then index
+ * mapping, as described above.  Output as var_block_mask_build: row_ptr
+ * [(side/8)^2 + 1], entries (sorted per row), sink_len; call with entries =
+ * NULL to get *nnz_out for sizing.  step >= decision_step; the target side a
+ * multiple of 8.  Errors: VAR_ERR_INVALID_ARG (arguments, entries_cap too
+ * small), VAR_ERR_UNSUPPORTED (sides).
+ */
+VAR_API int var_sparvar_mask_build(const var_problem* p, int32_t decision_step, int32_t step,
+                                   int32_t sink_max_side, const double* scores, double tau,
+                                   int32_t* row_ptr, int32_t* entries, int32_t entries_cap,
+                                   int32_t* nnz_out, int32_t* n_qblocks_out, int32_t* sink_len_out);
+
 /* floor(n * num / den) in exact integer arithmetic (the kept-query count). */
 VAR_API int32_t var_keep_count(int32_t n, int32_t num, int32_t den);
 

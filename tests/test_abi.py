@@ -195,3 +195,52 @@ def test_block_mask_rejects_bad_shapes():
     q = V.problem(1, 1, 64, (1, 32, 4, 64))
     with pytest.raises(V.VarError):
         V.var_block_mask_build(q, 3, 8, 1, 4)       # a sink scale after a non-sink one
+
+
+# ---------------------------------------------------------------- dynamic pattern (SparVAR)
+
+@pytest.mark.parametrize("sides,d,k_step,sink", [
+    ((1, 2, 4, 6, 8, 12, 16, 20, 24, 32, 40, 48, 64), 9, 12, 16),     # 1024px: 32x32 decides 64x64
+    ((1, 2, 4, 6, 8, 12, 16, 20, 24, 32, 40, 48, 64), 11, 12, 16),    # 48 -> 64 (non-integer ratio)
+    ((1, 2, 4, 6, 8, 12, 16, 20, 24, 32, 40, 48, 64), 9, 9, 16),      # the decision step itself
+    ((1, 2, 4, 8, 16, 24, 32), 4, 6, 4),
+])
+def test_sparvar_mask_equals_oracle(sides, d, k_step, sink):
+    p = V.problem(1, 1, 64, sides)
+    U, n_sink = V.var_sparvar_units(p, d, sink)
+    unit_of, units, ns = oracle.sparvar_units(sides, d, sink)
+    assert (U, n_sink) == (len(units), ns)
+    nqb = (sides[d] // 8) ** 2
+    rng = np.random.default_rng(901 + d)
+    A = rng.random((nqb, U)) ** 3
+    A[:, n_sink + 2] = A[:, n_sink + 1]                 # equal scores: the lower unit goes first
+    A /= A.sum(axis=1, keepdims=True)
+    for tau in (0.0, 0.3, 0.8, 1.0):
+        rp, en, sink_len = V.var_sparvar_mask_build(p, d, k_step, sink, A, tau)
+        got = _csr_to_token_mask(sides, k_step, 8, rp, en, sink_len)
+        kept = oracle.sparvar_select(A, ns, tau)
+        ref = oracle.sparvar_keep_mask(sides, d, k_step, units, kept, sink)
+        assert np.array_equal(got, ref.astype(bool)), tau
+        for qb in range(len(rp) - 1):                   # sorted, unique rows
+            row = en[rp[qb]:rp[qb + 1]]
+            assert np.all(np.diff(row) > 0)
+
+
+def test_sparvar_rejects_bad_arguments():
+    sides = (1, 2, 4, 6, 8, 12, 16, 20, 24, 32, 40, 48, 64)
+    p = V.problem(2, 16, 128, sides)
+    A = np.full((16, 43), 1.0 / 43)
+    with pytest.raises(V.VarError):
+        V.var_sparvar_units(p, 7, 16)                   # side 20 is not a multiple of 8
+    with pytest.raises(V.VarError):
+        V.var_sparvar_units(p, 6, 16)                   # side 16 is a sink scale
+    with pytest.raises(V.VarError):
+        V.var_sparvar_mask_build(p, 9, 8, 16, A, 0.5)   # target before the decision step
+    with pytest.raises(V.VarError):
+        V.var_sparvar_mask_build(p, 9, 12, 16, A, 1.5)  # tau outside [0, 1]
+    q = V.problem(2, 16, 128, (1, 2, 4, 8, 16, 24, 36))
+    with pytest.raises(V.VarError):
+        V.var_sparvar_mask_build(q, 5, 6, 4, np.full((9, 15), 1 / 15), 0.5)   # target side 36
+    L = V.lib()
+    assert L.var_sparvar_workspace_bytes(None, 9) == 0
+    assert L.var_sparvar_scores(C.byref(p), 9, 16, None, None, None, 0, None, None) == V.VAR_ERR_INVALID_ARG

@@ -81,6 +81,11 @@ _SIGS = {
                                       _P, _P]),
     "var_attn_blocksparse": (C.c_int, [_PROB, C.c_int32, _P, _P, _P,
                                        C.POINTER(var_block_mask), _P, _P]),
+    "var_sparvar_units": (C.c_int, [_PROB, C.c_int32, C.c_int32, _P, _P]),
+    "var_sparvar_workspace_bytes": (C.c_size_t, [_PROB, C.c_int32]),
+    "var_sparvar_scores": (C.c_int, [_PROB, C.c_int32, C.c_int32, _P, _P, _P, C.c_size_t, _P, _P]),
+    "var_sparvar_mask_build": (C.c_int, [_PROB, C.c_int32, C.c_int32, C.c_int32, _P, C.c_double, _P, _P,
+                                         C.c_int32, _P, _P, _P]),
     "var_keep_count": (C.c_int32, [C.c_int32, C.c_int32, C.c_int32]),
     "var_status_string": (C.c_char_p, [C.c_int]),
     "var_device_status": (C.c_int, [_P, C.c_int32]),
@@ -222,6 +227,44 @@ def var_guided_pivot_select(p: var_problem, step: int, src_step: int, sal: torch
            _lib.var_guided_pivot_select(C.byref(p), step, src_step, _ptr(sal), keep_k, _ptr(idx), _ptr(scores),
                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
                                         _stream(stream)))
+
+
+def var_sparvar_units(p: var_problem, decision_step: int, sink_max_side: int) -> Tuple[int, int]:
+    """Host call: (U, n_sink) -- the decision step's 64-key units and how many are sink chunks."""
+    u, ns = C.c_int32(), C.c_int32()
+    _check("var_sparvar_units", _lib.var_sparvar_units(C.byref(p), decision_step, sink_max_side, C.byref(u),
+                                                       C.byref(ns)))
+    return u.value, ns.value
+
+
+def var_sparvar_workspace_bytes(p: var_problem, decision_step: int) -> int:
+    return _lib.var_sparvar_workspace_bytes(C.byref(p), decision_step)
+
+
+def var_sparvar_scores(p: var_problem, decision_step: int, sink_max_side: int, q: torch.Tensor, k: torch.Tensor,
+                       workspace: torch.Tensor, scores: torch.Tensor, stream=None) -> None:
+    """scores: device float64 [(side/8)^2, U]."""
+    _check("var_sparvar_scores",
+           _lib.var_sparvar_scores(C.byref(p), decision_step, sink_max_side, _ptr(q), _ptr(k), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _ptr(scores), _stream(stream)))
+
+
+def var_sparvar_mask_build(p: var_problem, decision_step: int, step: int, sink_max_side: int,
+                           scores: np.ndarray, tau: float) -> Tuple[np.ndarray, np.ndarray, int]:
+    """Host call: the target step's block mask (row_ptr, entries, sink_len) from the
+    decision step's scores (host float64 [(side_d/8)^2, U])."""
+    sc = np.ascontiguousarray(scores, dtype=np.float64)
+    nnz, nqb, sink = C.c_int32(), C.c_int32(), C.c_int32()
+    _check("var_sparvar_mask_build",
+           _lib.var_sparvar_mask_build(C.byref(p), decision_step, step, sink_max_side, sc.ctypes.data, tau, None,
+                                       None, 0, C.byref(nnz), C.byref(nqb), C.byref(sink)))
+    row_ptr = np.zeros(nqb.value + 1, dtype=np.int32)
+    entries = np.zeros(max(1, nnz.value), dtype=np.int32)
+    _check("var_sparvar_mask_build",
+           _lib.var_sparvar_mask_build(C.byref(p), decision_step, step, sink_max_side, sc.ctypes.data, tau,
+                                       row_ptr.ctypes.data, entries.ctypes.data, entries.size, C.byref(nnz),
+                                       C.byref(nqb), C.byref(sink)))
+    return row_ptr, entries[: nnz.value], sink.value
 
 
 def var_restore_scatter(p: var_problem, step: int, prev: torch.Tensor, o_compact: Optional[torch.Tensor],

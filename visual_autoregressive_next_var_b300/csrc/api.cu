@@ -386,6 +386,159 @@ int var_block_mask_plan(const var_problem* p, int32_t step, int32_t qblock_side,
     return VAR_OK;
 }
 
+// ---------------------------------------------------------------- dynamic sparse pattern
+
+namespace {
+
+// The decision step's units (see UnitMap).  The decision scale must be a
+// non-sink scale whose side is a multiple of 8, and the sink scales a prefix.
+int build_unit_map(const var_problem* p, int32_t d, int32_t sink_max_side, varattn::UnitMap* m)
+{
+    using namespace varattn;
+    StepGeom g;
+    if (int rc = resolve(p, d, &g)) return rc;
+    if (sink_max_side < 0) return VAR_ERR_INVALID_ARG;
+    if (g.side % 8 != 0 || g.side <= sink_max_side) return VAR_ERR_UNSUPPORTED;
+    *m = UnitMap{};
+    m->L = g.L;
+    int sc = 0, off = 0;
+    while (sc <= d && p->side[sc] <= sink_max_side) {
+        off += p->side[sc] * p->side[sc];
+        ++sc;
+    }
+    m->sink_len = off;
+    m->n_sink = (off + 63) / 64;
+    int u = m->n_sink;
+    for (; sc <= d; ++sc) {
+        const int s = p->side[sc];
+        if (s <= sink_max_side) return VAR_ERR_UNSUPPORTED;   // a sink scale after a non-sink one
+        const int nbs = (s + 7) / 8;
+        if (nbs > 4095) return VAR_ERR_UNSUPPORTED;
+        m->sc[m->n_sc] = sc;
+        m->off[m->n_sc] = off;
+        m->side[m->n_sc] = s;
+        m->ubase[m->n_sc] = u;
+        ++m->n_sc;
+        u += nbs * nbs;
+        off += s * s;
+    }
+    m->U = u;
+    return VAR_OK;
+}
+
+}  // namespace
+
+int var_sparvar_units(const var_problem* p, int32_t decision_step, int32_t sink_max_side, int32_t* n_units_out,
+                      int32_t* n_sink_units_out)
+{
+    varattn::UnitMap m;
+    if (int rc = build_unit_map(p, decision_step, sink_max_side, &m)) return rc;
+    if (n_units_out) *n_units_out = m.U;
+    if (n_sink_units_out) *n_sink_units_out = m.n_sink;
+    return VAR_OK;
+}
+
+size_t var_sparvar_workspace_bytes(const var_problem* p, int32_t decision_step)
+{
+    StepGeom g;
+    if (resolve(p, decision_step, &g)) return 0;
+    return varattn::sparvar_workspace_bytes(g);
+}
+
+int var_sparvar_scores(const var_problem* p, int32_t decision_step, int32_t sink_max_side, const void* q,
+                       const void* k, void* workspace, size_t workspace_bytes, double* scores, void* stream)
+{
+    StepGeom g;
+    if (int rc = resolve(p, decision_step, &g)) return rc;
+    varattn::UnitMap m;
+    if (int rc = build_unit_map(p, decision_step, sink_max_side, &m)) return rc;
+    if (!q || !k || !workspace || !scores) return VAR_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(scores) & 7))
+        return VAR_ERR_UNSUPPORTED;
+    return varattn::launch_sparvar_scores(g, m, q, k, workspace, workspace_bytes, scores,
+                                          static_cast<cudaStream_t>(stream));
+}
+
+int var_sparvar_mask_build(const var_problem* p, int32_t decision_step, int32_t step, int32_t sink_max_side,
+                           const double* scores, double tau, int32_t* row_ptr, int32_t* entries,
+                           int32_t entries_cap, int32_t* nnz_out, int32_t* n_qblocks_out, int32_t* sink_len_out)
+{
+    varattn::UnitMap m;
+    if (int rc = build_unit_map(p, decision_step, sink_max_side, &m)) return rc;
+    StepGeom gk;
+    if (int rc = resolve(p, step, &gk)) return rc;
+    if (step < decision_step || !scores || !(tau >= 0.0 && tau <= 1.0)) return VAR_ERR_INVALID_ARG;
+    if (gk.side % 8 != 0) return VAR_ERR_UNSUPPORTED;
+    for (int sc = decision_step + 1; sc <= step; ++sc)
+        if ((p->side[sc] + 7) / 8 > 4095) return VAR_ERR_UNSUPPORTED;
+    const int s_d = p->side[decision_step];
+    const int nb_d = s_d / 8, nb_k = gk.side / 8;
+    const int n_qb_d = nb_d * nb_d;
+    // Selection per decision block: the sinks, then the other units by decreasing
+    // score (equal scores: lower unit first) until the kept mass, added in fp64 in
+    // that order, reaches tau of the row's total (added in unit order).
+    std::vector<std::vector<int32_t>> blocks(n_qb_d);     // the kept blocks' entries per decision block
+    std::vector<int> order(m.U - m.n_sink);
+    for (int qb = 0; qb < n_qb_d; ++qb) {
+        const double* row = scores + static_cast<size_t>(qb) * m.U;
+        double total = 0.0, have = 0.0;
+        for (int u = 0; u < m.U; ++u) total += row[u];
+        for (int u = 0; u < m.n_sink; ++u) have += row[u];
+        for (int i = 0; i < m.U - m.n_sink; ++i) order[i] = m.n_sink + i;
+        std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return row[a] > row[b]; });
+        std::vector<int32_t>& out = blocks[qb];
+        for (int u : order) {
+            if (have >= tau * total) break;
+            have += row[u];
+            // unit u -> (scale, block row, block column)
+            int t = 0;
+            while (t + 1 < m.n_sc && u >= m.ubase[t + 1]) ++t;
+            const int s = m.side[t], nbs = (s + 7) / 8;
+            const int bu = (u - m.ubase[t]) / nbs, bv = (u - m.ubase[t]) % nbs;
+            const int sc = m.sc[t];
+            if (sc < decision_step) {
+                out.push_back((sc << 24) | (bu << 12) | bv);
+                continue;
+            }
+            // a block of the decision scale: itself, and by index mapping the blocks of
+            // every later scale up to `step` that meet it rescaled (rounded outward)
+            const long long r0 = 8ll * bu, r1 = std::min(8ll * bu + 8, static_cast<long long>(s_d));
+            const long long c0 = 8ll * bv, c1 = std::min(8ll * bv + 8, static_cast<long long>(s_d));
+            for (int sc2 = decision_step; sc2 <= step; ++sc2) {
+                const long long s2 = p->side[sc2];
+                const long long lo_r = r0 * s2 / s_d, hi_r = (r1 * s2 + s_d - 1) / s_d;
+                const long long lo_c = c0 * s2 / s_d, hi_c = (c1 * s2 + s_d - 1) / s_d;
+                for (long long uu = lo_r / 8; uu < (hi_r + 7) / 8; ++uu)
+                    for (long long vv = lo_c / 8; vv < (hi_c + 7) / 8; ++vv)
+                        out.push_back(static_cast<int32_t>((sc2 << 24) | (uu << 12) | vv));
+            }
+        }
+        std::sort(out.begin(), out.end());
+        out.erase(std::unique(out.begin(), out.end()), out.end());
+    }
+    // Index mapping of the query blocks: target block (by, bx) takes the decision
+    // block under its centre.
+    long long nnz = 0;
+    for (int qb = 0; qb < nb_k * nb_k; ++qb) {
+        const int by = qb / nb_k, bx = qb % nb_k;
+        const int dy = static_cast<int>((2ll * by + 1) * nb_d / (2ll * nb_k));
+        const int dx = static_cast<int>((2ll * bx + 1) * nb_d / (2ll * nb_k));
+        const std::vector<int32_t>& src = blocks[dy * nb_d + dx];
+        if (row_ptr) row_ptr[qb] = static_cast<int32_t>(nnz);
+        if (entries) {
+            if (nnz + static_cast<long long>(src.size()) > entries_cap) return VAR_ERR_INVALID_ARG;
+            std::copy(src.begin(), src.end(), entries + nnz);
+        }
+        nnz += static_cast<long long>(src.size());
+        if (nnz > 0x7fffffffll) return VAR_ERR_UNSUPPORTED;
+    }
+    if (row_ptr) row_ptr[nb_k * nb_k] = static_cast<int32_t>(nnz);
+    if (nnz_out) *nnz_out = static_cast<int32_t>(nnz);
+    if (n_qblocks_out) *n_qblocks_out = nb_k * nb_k;
+    if (sink_len_out) *sink_len_out = m.sink_len;
+    return VAR_OK;
+}
+
 int var_attn_blocksparse(const var_problem* p, int32_t step, const void* q, const void* k,
                          const void* v, const var_block_mask* mask, void* o, void* stream)
 {

@@ -39,6 +39,9 @@ int encode_tmap_bf16(CUtensorMap* out, const void* base, int rank, const uint64_
 
 int launch_attn_dense(const StepGeom& g, const void* q, const void* k, const void* v, void* o,
                       cudaStream_t st, float* lse = nullptr);
+// As launch_attn_dense with V read at its own stride of v_cap rows per (b,h).
+int launch_attn_dense_vcap(const StepGeom& g, const void* q, const void* k, const void* v, int v_cap, void* o,
+                           cudaStream_t st);
 int launch_attn_pruned(const StepGeom& g, const void* q, const void* k, const void* v,
                        const int32_t* idx, int keep_k, void* o, cudaStream_t st, bool scatter);
 int launch_attn_dense_halved(const StepGeom& g, const void* q, const void* k, const void* v, void* o,
@@ -56,6 +59,19 @@ int launch_saliency(const StepGeom& g, int n_src, int L_src, const void* q, cons
 size_t guided_workspace_bytes(int B, int N);
 int launch_guided_pivot(int B, int H, int sp, int s, const float* sal, int keep_k, int32_t* idx, float* scores,
                         void* ws, size_t ws_bytes, cudaStream_t st);
+// The decision step's 64-key units (dynamic sparse pattern): the sink range
+// [0, sink_len) in 64-token chunks (units [0, n_sink)), then every 8x8 key block
+// of each later scale up to the decision scale, row-major, scale by scale.
+struct UnitMap {
+    int L, U, sink_len, n_sink, n_sc;
+    int sc[VAR_MAX_SCALES];      // schedule index of each non-sink scale
+    int off[VAR_MAX_SCALES];     // its first flat key
+    int side[VAR_MAX_SCALES];
+    int ubase[VAR_MAX_SCALES];   // its first unit
+};
+size_t sparvar_workspace_bytes(const StepGeom& g);
+int launch_sparvar_scores(const StepGeom& g, const UnitMap& m, const void* q, const void* k, void* ws,
+                          size_t ws_bytes, double* scores, cudaStream_t st);
 int launch_restore_scatter(int B, int H, int D, int sp, int s, const void* prev, const void* oc,
                            const int32_t* idx, int keep_k, void* out, cudaStream_t st, bool fill_only);
 
