@@ -427,6 +427,32 @@ def extra_rows(V, dev, step: Step, iters: int, peaks):
         "note": f"source step 32x32 ({Ns} queries, {L_src} keys) -> 64x64, keep 1/5; the row "
                 "statistics are written by the source step's own dense attention",
         "timing": "CUDA graph replay after an L2 flush"}
+    # SparVAR dynamic pattern: the 32x32 step's block scores decide the 64x64 step's mask
+    d_sv, tau_sv = FINAL - 3, 0.8
+    U_sv, _ = step.V.var_sparvar_units(step.p, d_sv, SINK_SIDE)
+    sv_ws = torch.empty(step.V.var_sparvar_workspace_bytes(step.p, d_sv), dtype=torch.uint8, device=dev)
+    nqb_sv = (int(round(step.q_src.shape[2] ** 0.5)) // 8) ** 2
+    sv_sc = torch.empty((nqb_sv, U_sv), dtype=torch.float64, device=dev)
+    t_sc = time_graph(lambda: step.V.var_sparvar_scores(step.p, d_sv, SINK_SIDE, step.q_src, step.k, sv_ws, sv_sc),
+                      iters, flush)
+    t0 = time.perf_counter()
+    A = sv_sc.cpu().numpy()
+    rp, en, sink = step.V.var_sparvar_mask_build(step.p, d_sv, FINAL, SINK_SIDE, A, tau_sv)
+    sv_plan = [torch.as_tensor(a, device=dev) for a in step.V.var_block_mask_plan(step.p, FINAL, QBLOCK, rp, en, sink)]
+    t_host = (time.perf_counter() - t0) * 1e3
+    sv_rp, sv_en = torch.as_tensor(rp, device=dev), torch.as_tensor(en, device=dev)
+    sv_mask = step.V.block_mask_struct(QBLOCK, sv_rp, sv_en, sink, sv_plan)
+    t_sv = time_graph(lambda: step.V.var_attn_blocksparse(step.p, FINAL, step.q, step.k, step.v, sv_mask,
+                                                           step.o_sparse), iters, flush)
+    pairs = mask_kept_pairs(WORKLOADS[STEP_WORKLOAD].sides, rp, en, sink, QBLOCK)
+    fl_sv = 4.0 * step.q.shape[0] * step.q.shape[1] * pairs * step.q.shape[3]
+    rows["sparvar_dynamic_mask_32_to_64"] = {
+        "scores_ms": t_sc, "host_select_map_plan_ms": t_host, "attn_ms": t_sv,
+        "density": pairs / (step.N * step.L), "TFLOP/s": fl_sv / t_sv / 1e9,
+        "dense_equiv_TFLOP/s": step.flops_dense / t_sv / 1e9, "units": U_sv, "tau": tau_sv,
+        "note": "decision step 32x32: block scores (dense attention on unit-indicator values, "
+                f"{U_sv} units) -> host selection + index mapping -> block-sparse attention of the 64x64 step",
+        "timing": "CUDA graph replay after an L2 flush; host part timed once"}
     # Branch Halving: the conditional half only, its rows repeated
     t = time_graph(lambda: step.V.var_attn_dense_halved(step.p, FINAL, step.q, step.k, step.v, step.o_dense),
                    iters, flush)
