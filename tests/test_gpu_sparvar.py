@@ -94,3 +94,25 @@ def test_dynamic_mask_1024px_decision_32_target_64():
     ref = oracle.attention_keep(q[:, :, torch.as_tensor(rows)].contiguous(), inp.k, inp.v, L, keep[rows])
     assert_close(o[:, :, torch.as_tensor(rows, device=DEV)], ref, "dynamic mask 1024px")
     check_device_status()
+
+
+def test_dynamic_mask_head_dim_64_single_batch():
+    B, H, D, sink, d, ks, tau = 1, 3, 64, 4, 6, 8, 0.7        # 32 x 32 decides the 48 x 48 step
+    L = cache_len(SMALL, ks)
+    q_d = randn_bf16((B, H, SMALL[d] ** 2, D), 1121)
+    q = randn_bf16((B, H, SMALL[ks] ** 2, D), 1122)
+    k = randn_bf16((B, H, L, D), 1123)
+    v = randn_bf16((B, H, L, D), 1124)
+    p = V.problem(B, H, D, SMALL, kv_capacity=L)
+    kd, vd = k.to(DEV), v.to(DEV)
+    A = gpu_scores(p, d, sink, q_d.to(DEV), kd)
+    check_scores(A, oracle.sparvar_scores(q_d, k, SMALL, d, sink))
+    rp, en, sink_len = V.var_sparvar_mask_build(p, d, ks, sink, A, tau)
+    mask = V.block_mask_struct(8, torch.as_tensor(rp, device=DEV), torch.as_tensor(en, device=DEV), sink_len)
+    o = torch.empty_like(q, device=DEV)
+    V.var_attn_blocksparse(p, ks, q.to(DEV), kd, vd, mask, o)   # without a plan: the kernel merges the lists
+    torch.cuda.synchronize()
+    _, units, ns = oracle.sparvar_units(SMALL, d, sink)
+    keep = oracle.sparvar_keep_mask(SMALL, d, ks, units, oracle.sparvar_select(A, ns, tau), sink)
+    assert_close(o, oracle.attention_keep(q, k, v, L, keep), "dynamic mask D 64")
+    check_device_status()
