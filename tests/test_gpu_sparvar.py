@@ -116,3 +116,17 @@ def test_dynamic_mask_head_dim_64_single_batch():
     keep = oracle.sparvar_keep_mask(SMALL, d, ks, units, oracle.sparvar_select(A, ns, tau), sink)
     assert_close(o, oracle.attention_keep(q, k, v, L, keep), "dynamic mask D 64")
     check_device_status()
+
+
+def test_scores_two_passes_head_dim_128():
+    sides, sink, d = (1, 2, 4, 8, 16, 24, 32, 40, 48, 64), 4, 9        # 156 units > 128: two passes
+    B, H, D = 1, 1, 128
+    L, N = cache_len(sides, d), sides[d] ** 2
+    q = randn_bf16((B, H, N, D), 1131)
+    k = randn_bf16((B, H, L, D), 1132)
+    p = V.problem(B, H, D, sides)
+    U, _ = V.var_sparvar_units(p, d, sink)
+    assert U > 128
+    got = gpu_scores(p, d, sink, q.to(DEV), k.to(DEV))
+    check_scores(got, oracle.sparvar_scores(q, k, sides, d, sink))
+    check_device_status()
