@@ -91,11 +91,20 @@ def load_peaks():
             "source": "fallback"}
 
 
+# The sources that decide what the attention kernels do and launch: the kernel,
+# its PTX wrappers, the shared header, both launchers and the public header.
+ATTN_SOURCES = ("visual_autoregressive_next_var_b300/csrc/attn_kernel.cuh",
+                "visual_autoregressive_next_var_b300/csrc/ptx.cuh",
+                "visual_autoregressive_next_var_b300/csrc/internal.h",
+                "visual_autoregressive_next_var_b300/csrc/attn.cu",
+                "visual_autoregressive_next_var_b300/csrc/blocksparse.cu",
+                "include/varattn.h")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "visual_autoregressive_next_var_b300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in ATTN_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
     return h.hexdigest()[:16]
 
 

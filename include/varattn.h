@@ -390,6 +390,16 @@ VAR_API int var_sparvar_mask_build(const var_problem* p, int32_t decision_step, 
                                    int32_t* row_ptr, int32_t* entries, int32_t entries_cap,
                                    int32_t* nnz_out, int32_t* n_qblocks_out, int32_t* sink_len_out);
 
+/*
+ * Diagnostics: launch a one-thread kernel whose bounded wait on a barrier that
+ * nothing arrives on gives up after limit_us microseconds (1 .. 10^7) and
+ * records VAR_ERR_TIMEOUT in the device status word, exactly as a pipeline
+ * wait of the kernels above that gave up would.  It lets a caller check the
+ * failure path (var_device_status) without a fault: the device stays usable.
+ * Asynchronous on `stream`.  Errors: VAR_ERR_INVALID_ARG, VAR_ERR_CUDA.
+ */
+VAR_API int var_selftest_wait_timeout(int32_t limit_us, void* stream);
+
 /* floor(n * num / den) in exact integer arithmetic (the kept-query count). */
 VAR_API int32_t var_keep_count(int32_t n, int32_t num, int32_t den);
 

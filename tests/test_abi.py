@@ -244,3 +244,9 @@ def test_sparvar_rejects_bad_arguments():
     L = V.lib()
     assert L.var_sparvar_workspace_bytes(None, 9) == 0
     assert L.var_sparvar_scores(C.byref(p), 9, 16, None, None, None, 0, None, None) == V.VAR_ERR_INVALID_ARG
+
+
+def test_selftest_wait_timeout_rejects_bad_limits():
+    L = V.lib()
+    assert L.var_selftest_wait_timeout(0, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_selftest_wait_timeout(10000001, None) == V.VAR_ERR_INVALID_ARG

@@ -86,6 +86,7 @@ _SIGS = {
     "var_sparvar_scores": (C.c_int, [_PROB, C.c_int32, C.c_int32, _P, _P, _P, C.c_size_t, _P, _P]),
     "var_sparvar_mask_build": (C.c_int, [_PROB, C.c_int32, C.c_int32, C.c_int32, _P, C.c_double, _P, _P,
                                          C.c_int32, _P, _P, _P]),
+    "var_selftest_wait_timeout": (C.c_int, [C.c_int32, _P]),
     "var_keep_count": (C.c_int32, [C.c_int32, C.c_int32, C.c_int32]),
     "var_status_string": (C.c_char_p, [C.c_int]),
     "var_device_status": (C.c_int, [_P, C.c_int32]),
@@ -227,6 +228,11 @@ def var_guided_pivot_select(p: var_problem, step: int, src_step: int, sal: torch
            _lib.var_guided_pivot_select(C.byref(p), step, src_step, _ptr(sal), keep_k, _ptr(idx), _ptr(scores),
                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
                                         _stream(stream)))
+
+
+def var_selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    """Diagnostics: a kernel whose bounded wait gives up and records VAR_ERR_TIMEOUT."""
+    _check("var_selftest_wait_timeout", _lib.var_selftest_wait_timeout(limit_us, _stream(stream)))
 
 
 def var_sparvar_units(p: var_problem, decision_step: int, sink_max_side: int) -> Tuple[int, int]:

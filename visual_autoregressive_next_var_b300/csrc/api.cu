@@ -428,6 +428,12 @@ int build_unit_map(const var_problem* p, int32_t d, int32_t sink_max_side, varat
 
 }  // namespace
 
+int var_selftest_wait_timeout(int32_t limit_us, void* stream)
+{
+    if (limit_us <= 0 || limit_us > 10000000) return VAR_ERR_INVALID_ARG;
+    return varattn::launch_wait_timeout(limit_us, static_cast<cudaStream_t>(stream));
+}
+
 int var_sparvar_units(const var_problem* p, int32_t decision_step, int32_t sink_max_side, int32_t* n_units_out,
                       int32_t* n_sink_units_out)
 {

@@ -70,6 +70,8 @@ struct UnitMap {
     int ubase[VAR_MAX_SCALES];   // its first unit
 };
 size_t sparvar_workspace_bytes(const StepGeom& g);
+// One-thread kernel whose wait gives up after limit_us and records VAR_ERR_TIMEOUT.
+int launch_wait_timeout(int limit_us, cudaStream_t st);
 int launch_sparvar_scores(const StepGeom& g, const UnitMap& m, const void* q, const void* k, void* ws,
                           size_t ws_bytes, double* scores, cudaStream_t st);
 int launch_restore_scatter(int B, int H, int D, int sp, int s, const void* prev, const void* oc,
