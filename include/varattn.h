@@ -84,6 +84,14 @@ VAR_API int var_attn_dense(const var_problem* p, int32_t step, const void* q, co
 VAR_API size_t var_pivot_workspace_bytes(const var_problem* p, int32_t step, int32_t channels);
 
 /*
+ * Device workspace bytes the path's calls need at `step` with `channels` hidden
+ * channels and keep_k kept queries: pivot selection is the only one that takes
+ * scratch, so this is var_pivot_workspace_bytes (0 for invalid arguments,
+ * keep_k outside [0, N] included).
+ */
+VAR_API size_t var_workspace_bytes(const var_problem* p, int32_t step, int32_t channels, int32_t keep_k);
+
+/*
  * Pivot selection for cached token pruning ("FastVAR: Linear Visual
  * Autoregressive Modeling via Cached Token Pruning", abstract: only pivotal
  * tokens are forwarded; "ARVAR" Key Design 2: Top-K indices gather the tokens).

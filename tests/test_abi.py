@@ -250,3 +250,10 @@ def test_selftest_wait_timeout_rejects_bad_limits():
     L = V.lib()
     assert L.var_selftest_wait_timeout(0, None) == V.VAR_ERR_INVALID_ARG
     assert L.var_selftest_wait_timeout(10000001, None) == V.VAR_ERR_INVALID_ARG
+
+
+def test_workspace_bytes_is_the_pivot_scratch():
+    p = V.problem(2, 16, 128, SCHEDULE_1024)
+    assert V.var_workspace_bytes(p, 12, 2048, 819) == V.var_pivot_workspace_bytes(p, 12, 2048) > 0
+    assert V.var_workspace_bytes(p, 12, 2048, 4097) == 0       # keep_k above N
+    assert V.var_workspace_bytes(p, 12, 2048, -1) == 0

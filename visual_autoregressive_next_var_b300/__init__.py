@@ -87,6 +87,7 @@ _SIGS = {
     "var_sparvar_mask_build": (C.c_int, [_PROB, C.c_int32, C.c_int32, C.c_int32, _P, C.c_double, _P, _P,
                                          C.c_int32, _P, _P, _P]),
     "var_selftest_wait_timeout": (C.c_int, [C.c_int32, _P]),
+    "var_workspace_bytes": (C.c_size_t, [_PROB, C.c_int32, C.c_int32, C.c_int32]),
     "var_keep_count": (C.c_int32, [C.c_int32, C.c_int32, C.c_int32]),
     "var_status_string": (C.c_char_p, [C.c_int]),
     "var_device_status": (C.c_int, [_P, C.c_int32]),
@@ -228,6 +229,11 @@ def var_guided_pivot_select(p: var_problem, step: int, src_step: int, sal: torch
            _lib.var_guided_pivot_select(C.byref(p), step, src_step, _ptr(sal), keep_k, _ptr(idx), _ptr(scores),
                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
                                         _stream(stream)))
+
+
+def var_workspace_bytes(p: var_problem, step: int, channels: int, keep_k: int) -> int:
+    """Device workspace bytes the path's calls need at `step` (pivot selection's scratch)."""
+    return _lib.var_workspace_bytes(C.byref(p), step, channels, keep_k)
 
 
 def var_selftest_wait_timeout(limit_us: int, stream=None) -> None:

@@ -428,6 +428,13 @@ int build_unit_map(const var_problem* p, int32_t d, int32_t sink_max_side, varat
 
 }  // namespace
 
+size_t var_workspace_bytes(const var_problem* p, int32_t step, int32_t channels, int32_t keep_k)
+{
+    StepGeom g;
+    if (resolve(p, step, &g) || keep_k < 0 || keep_k > g.N) return 0;
+    return var_pivot_workspace_bytes(p, step, channels);
+}
+
 int var_selftest_wait_timeout(int32_t limit_us, void* stream)
 {
     if (limit_us <= 0 || limit_us > 10000000) return VAR_ERR_INVALID_ARG;
