@@ -1,22 +1,29 @@
 #!/usr/bin/env python3
 """Benchmark of the next-scale VAR attention hot path on B300.
 
-One step = the final scale of the 1024px schedule (64x64 = 4,096 queries of a
-CFG pair, 16 heads, head_dim 128, attending a 10,521-token cache) taken
-through every row of the hot path, all through the C ABI:
-  dense attention      var_attn_dense
-  pivot selection      var_pivot_select      (hidden states 4096 x 2048, keep 20 %)
-  pruned attention     var_attn_pruned
-  restore + scatter    var_restore_scatter   (from the 48x48 step's output)
-  block-sparse         var_attn_blocksparse  (sinks <= 16, +-2 block window;
-                                              the mask is built once on the host)
-`value` is the step's dense-equivalent TFLOP/s: the dense FLOPs of the three
-attention variants (each computes the final-scale attention) divided by the
-step time.  The JSON line also carries:
+One step = one pass of every row of the path, each on its workload, all
+through the C ABI:
+  dense attention      var_attn_dense         1024px final scale: 2 x 16 heads x
+                                              4,096 queries against 10,521 keys, D 128
+  cached token pruning var_pivot_select       the 48x48 step (hidden states 2304 x 2048,
+                       var_attn_pruned        keep 2/5), from the 40x40 step's output,
+                       var_restore_scatter    then the 64x64 step (4096 x 2048, keep
+                                              1/5) from the restored 48x48 output
+  block-sparse         var_attn_blocksparse   2K final scale: 16,384 queries against
+                                              42,521 keys, sinks <= 16 + a +-2 block
+                                              window (12.99 % of the pairs); the mask
+                                              and plan are built once on the host
+`value` is the step's algorithmic TFLOP/s: the FLOPs each attention kernel
+executes (4 D per computed (query, key) pair: every pair for dense, the kept
+rows for pruned, the kept pairs for block-sparse) over the step time.  The
+dense-equivalent "effective" figure (full dense FLOPs of every attention
+variant) is reported beside it, never against the peak.  The JSON line also
+carries:
   rows          per-kernel times inside the timed region (CUDA events between
                 the calls) and separate measurements: the small kernels from a
-                CUDA graph after an L2 flush, the 2K block-sparse workload, the
-                256px schedule
+                CUDA graph after an L2 flush, the fused pruned step, the
+                attention-guided pivots, the dynamic sparse pattern, Branch
+                Halving, the tiny and 256px workloads, the host link ceiling
   roofline      the step's dominant kernel against the measured peak
   e2e           the same step with host buffers (pinned H2D of its inputs, D2H
                 of its outputs, inside the timed region)
@@ -49,12 +56,22 @@ import torch  # noqa: E402
 from var_synth import WORKLOADS, cache_len, make_inputs  # noqa: E402
 
 METRIC = "final-scale attention ms and TFLOP/s (dense-equiv) at 1 B300; % of BF16 peak"
-STEP_WORKLOAD = "pruned_1024px"      # tensors of the 1024px schedule (CFG pair, sink) + hidden states
-FINAL = 12                           # the 64x64 step
-KEEP = (1, 5)                        # keep ratio at 64x64
+W1024 = "pruned_1024px"              # tensors of the 1024px schedule (CFG pair, sink) + hidden states
+W2K = "blocksparse_2k"
+PREV, MID, FINAL = 10, 11, 12        # the 40x40, 48x48 and 64x64 steps
+KEEP = {MID: (2, 5), FINAL: (1, 5)}  # keep ratios of the pruned steps
 QBLOCK, RADIUS, SINK_SIDE = 8, 2, 16
-ROW_NAMES = ("attn_dense", "pivot_select", "attn_pruned", "restore_scatter", "attn_blocksparse")
-LAUNCHES_PER_STEP = 7                # dense 1, pivot 3, pruned 1, restore 1, block-sparse 1
+ROW_NAMES = ("attn_dense_1024px", "pivot_select_48", "attn_pruned_48", "restore_scatter_40to48",
+             "pivot_select_64", "attn_pruned_64", "restore_scatter_48to64", "attn_blocksparse_2k")
+LAUNCHES_PER_STEP = 12               # dense 1, (pivot 3, pruned 1, restore 1) x 2, block-sparse 1
+KERNEL_NAMES = {"attn_dense_1024px": "attn_kernel<128, dense>", "attn_pruned_48": "attn_kernel<128, gather>",
+                "attn_pruned_64": "attn_kernel<128, gather>", "attn_blocksparse_2k": "attn_kernel<128, sparse>",
+                "pivot_select_48": "pivot kernels", "pivot_select_64": "pivot kernels",
+                "restore_scatter_40to48": "restore_scatter_kernel<128>",
+                "restore_scatter_48to64": "restore_scatter_kernel<128>"}
+TRAFFIC_KEYS = {"attn_dense_1024px": "attn_kernel<128, dense>:dense_1024px_final",
+                "attn_blocksparse_2k": "attn_kernel<128, sparse>:blocksparse_2k_final",
+                "attn_pruned_64": "attn_kernel<128, gather>:pruned_64x64_k819"}
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -91,14 +108,13 @@ def load_peaks():
             "source": "fallback"}
 
 
-# The sources that decide what the attention kernels do and launch: the kernel,
-# its PTX wrappers, the shared header, both launchers and the public header.
+# The sources that decide what the attention kernels compute and how they are
+# launched: the kernel body, its PTX wrappers and the two launchers (grid, CTA
+# plan, tensor maps).  Declarations elsewhere do not change the traffic.
 ATTN_SOURCES = ("visual_autoregressive_next_var_b300/csrc/attn_kernel.cuh",
                 "visual_autoregressive_next_var_b300/csrc/ptx.cuh",
-                "visual_autoregressive_next_var_b300/csrc/internal.h",
                 "visual_autoregressive_next_var_b300/csrc/attn.cu",
-                "visual_autoregressive_next_var_b300/csrc/blocksparse.cu",
-                "include/varattn.h")
+                "visual_autoregressive_next_var_b300/csrc/blocksparse.cu")
 
 
 def kernel_source_hash() -> str:
@@ -235,63 +251,101 @@ def time_graph(fn, iters: int, flush: L2Flush) -> float:
 # ----------------------------------------------------------------------------- the step
 
 class Step:
-    """Device buffers and the call sequence of one step."""
+    """Device buffers and the call sequence of one step (every row of the path)."""
 
-    def __init__(self, V, dev, inp):
-        w = WORKLOADS[STEP_WORKLOAD]
+    def __init__(self, V, dev, inp, inp2k, mask2k_host):
+        w, w2 = WORKLOADS[W1024], WORKLOADS[W2K]
         self.V = V
-        self.w = w
         B, H, D = w.batch, w.heads, w.head_dim
         self.p = V.problem(B, H, D, w.sides, kv_capacity=inp.k.shape[2])
-        self.N = w.sides[FINAL] ** 2
-        self.L = cache_len(w.sides, FINAL)
-        self.K = V.var_keep_count(self.N, *KEEP)
-        self.q = inp.q[FINAL].to(dev)
-        self.q_src = inp.q[FINAL - 3].to(dev)     # the 32x32 step whose attention guides the pivots
         self.k = inp.k.to(dev)
         self.v = inp.v.to(dev)
-        self.x = inp.x[FINAL].to(dev)
-        self.C = self.x.shape[2]
-        # the previous (48x48) step's output: dense attention, computed once
-        q11 = inp.q[FINAL - 1].to(dev)
-        self.prev = torch.empty_like(q11)
-        V.var_attn_dense(self.p, FINAL - 1, q11, self.k, self.v, self.prev)
-        del q11
-        self.o_dense = torch.empty_like(self.q)
-        self.ws = torch.empty(V.var_pivot_workspace_bytes(self.p, FINAL, self.C), dtype=torch.uint8, device=dev)
-        self.idx = torch.empty((B, self.K), dtype=torch.int32, device=dev)
-        self.oc = torch.empty((B, H, self.K, D), dtype=torch.bfloat16, device=dev)
-        self.o_pruned = torch.empty_like(self.q)
-        self.o_sparse = torch.empty_like(self.q)
-        t0 = time.perf_counter()
-        rp, en, sink = V.var_block_mask_build(self.p, FINAL, QBLOCK, RADIUS, SINK_SIDE)
-        self.rp = torch.as_tensor(rp, device=dev)
-        self.en = torch.as_tensor(en, device=dev)
-        self.plan = [torch.as_tensor(a, device=dev) for a in V.var_block_mask_plan(self.p, FINAL, QBLOCK, rp, en, sink)]
-        self.mask_build_ms = (time.perf_counter() - t0) * 1e3
-        self.mask = V.block_mask_struct(QBLOCK, self.rp, self.en, sink, self.plan)
-        self.sparse_pairs = mask_kept_pairs(w.sides, rp, en, sink, QBLOCK)
-        self.flops_dense = flops_attn(B, H, self.N, self.L, D)
-        self.flops_pruned = flops_attn(B, H, self.K, self.L, D)
-        self.flops_sparse = 4.0 * B * H * self.sparse_pairs * D
-        self.bytes_pivot = self.x.numel() * 2 + self.idx.numel() * 4
-        self.bytes_restore = (self.prev.numel() + self.oc.numel() + self.o_pruned.numel()) * 2 + self.idx.numel() * 4
+        self.q = {s: inp.q[s].to(dev) for s in (MID, FINAL)}
+        self.x = {s: inp.x[s].to(dev) for s in (MID, FINAL)}
+        self.N = {s: w.sides[s] ** 2 for s in (PREV, MID, FINAL)}
+        self.L = {s: cache_len(w.sides, s) for s in (PREV, MID, FINAL)}
+        self.K = {s: V.var_keep_count(self.N[s], *KEEP[s]) for s in (MID, FINAL)}
+        # the 40x40 step's output, the first restore's input: dense attention, computed once
+        q10 = inp.q[PREV].to(dev)
+        self.prev = torch.empty_like(q10)
+        V.var_attn_dense(self.p, PREV, q10, self.k, self.v, self.prev)
+        del q10
+        self.o_dense = torch.empty_like(self.q[FINAL])
+        C = self.x[FINAL].shape[2]
+        self.ws = {s: torch.empty(V.var_pivot_workspace_bytes(self.p, s, C), dtype=torch.uint8, device=dev)
+                   for s in (MID, FINAL)}
+        self.idx = {s: torch.empty((B, self.K[s]), dtype=torch.int32, device=dev) for s in (MID, FINAL)}
+        self.oc = {s: torch.empty((B, H, self.K[s], D), dtype=torch.bfloat16, device=dev) for s in (MID, FINAL)}
+        self.out = {s: torch.empty_like(self.q[s]) for s in (MID, FINAL)}
+        # 2K block-sparse
+        st2 = w2.steps[-1]
+        self.st2 = st2
+        self.p2 = V.problem(w2.batch, w2.heads, w2.head_dim, w2.sides)
+        self.q2, self.k2, self.v2 = inp2k.q[st2].to(dev), inp2k.k.to(dev), inp2k.v.to(dev)
+        self.o2 = torch.empty_like(self.q2)
+        rp, en, sink, plan = mask2k_host
+        self.mask_dev = [torch.as_tensor(rp, device=dev), torch.as_tensor(en, device=dev)] + \
+                        [torch.as_tensor(a, device=dev) for a in plan]
+        self.mask = V.block_mask_struct(QBLOCK, self.mask_dev[0], self.mask_dev[1], sink, self.mask_dev[2:])
+        self.sparse_pairs = mask_kept_pairs(w2.sides, rp, en, sink, QBLOCK)
+        self.N2, self.L2 = w2.sides[st2] ** 2, cache_len(w2.sides, st2)
+        # algorithmic work per row
+        self.flops = {
+            "attn_dense_1024px": flops_attn(B, H, self.N[FINAL], self.L[FINAL], D),
+            "attn_pruned_48": flops_attn(B, H, self.K[MID], self.L[MID], D),
+            "attn_pruned_64": flops_attn(B, H, self.K[FINAL], self.L[FINAL], D),
+            "attn_blocksparse_2k": 4.0 * w2.batch * w2.heads * self.sparse_pairs * w2.head_dim,
+        }
+        self.flops_dense_equiv = {
+            "attn_dense_1024px": self.flops["attn_dense_1024px"],
+            "attn_pruned_48": flops_attn(B, H, self.N[MID], self.L[MID], D),
+            "attn_pruned_64": flops_attn(B, H, self.N[FINAL], self.L[FINAL], D),
+            "attn_blocksparse_2k": flops_attn(w2.batch, w2.heads, self.N2, self.L2, w2.head_dim),
+        }
+        self.bytes = {
+            "pivot_select_48": self.x[MID].numel() * 2 + self.idx[MID].numel() * 4,
+            "pivot_select_64": self.x[FINAL].numel() * 2 + self.idx[FINAL].numel() * 4,
+            "restore_scatter_40to48": (self.prev.numel() + self.oc[MID].numel() + self.out[MID].numel()) * 2
+                                      + self.idx[MID].numel() * 4,
+            "restore_scatter_48to64": (self.out[MID].numel() + self.oc[FINAL].numel() + self.out[FINAL].numel()) * 2
+                                      + self.idx[FINAL].numel() * 4,
+        }
 
     def calls(self, stream=None):
         V, p = self.V, self.p
+
+        def pivot(s):
+            return lambda: V.var_pivot_select(p, s, self.x[s], self.K[s], self.idx[s], self.ws[s], stream=stream)
+
+        def pruned(s):
+            return lambda: V.var_attn_pruned(p, s, self.q[s], self.k, self.v, self.idx[s], self.K[s], self.oc[s],
+                                             stream=stream)
+
+        def restore(s, prev):
+            return lambda: V.var_restore_scatter(p, s, prev, self.oc[s], self.idx[s], self.K[s], self.out[s],
+                                                 stream=stream)
+
         return (
-            lambda: V.var_attn_dense(p, FINAL, self.q, self.k, self.v, self.o_dense, stream=stream),
-            lambda: V.var_pivot_select(p, FINAL, self.x, self.K, self.idx, self.ws, stream=stream),
-            lambda: V.var_attn_pruned(p, FINAL, self.q, self.k, self.v, self.idx, self.K, self.oc, stream=stream),
-            lambda: V.var_restore_scatter(p, FINAL, self.prev, self.oc, self.idx, self.K, self.o_pruned,
-                                          stream=stream),
-            lambda: V.var_attn_blocksparse(p, FINAL, self.q, self.k, self.v, self.mask, self.o_sparse,
+            lambda: V.var_attn_dense(p, FINAL, self.q[FINAL], self.k, self.v, self.o_dense, stream=stream),
+            pivot(MID), pruned(MID), restore(MID, self.prev),
+            pivot(FINAL), pruned(FINAL), restore(FINAL, self.out[MID]),
+            lambda: V.var_attn_blocksparse(self.p2, self.st2, self.q2, self.k2, self.v2, self.mask, self.o2,
                                            stream=stream),
         )
 
     def run(self, stream=None):
         for c in self.calls(stream):
             c()
+
+    def uploads(self, host):
+        """(device tensor, pinned host tensor) pairs of the step's inputs."""
+        return [(self.q[FINAL], host["q64"]), (self.q[MID], host["q48"]), (self.k, host["k"]), (self.v, host["v"]),
+                (self.x[MID], host["x48"]), (self.x[FINAL], host["x64"]), (self.prev, host["prev40"]),
+                (self.q2, host["q2k"]), (self.k2, host["k2k"]), (self.v2, host["v2k"])]
+
+    def results(self):
+        return {"o_dense": self.o_dense, "idx48": self.idx[MID], "idx64": self.idx[FINAL],
+                "out48": self.out[MID], "out64": self.out[FINAL], "o2k": self.o2}
 
 
 def time_step(step: Step, steps: int, stream):
@@ -310,13 +364,24 @@ def time_step(step: Step, steps: int, stream):
     return total, per_row
 
 
+def build_mask_2k(V):
+    """Host block mask and plan of the 2K final step: (row_ptr, entries, sink_len, plan), ms."""
+    w = WORKLOADS[W2K]
+    st = w.steps[-1]
+    p = V.problem(w.batch, w.heads, w.head_dim, w.sides)
+    t0 = time.perf_counter()
+    rp, en, sink = V.var_block_mask_build(p, st, w.qblock_side, w.radius, w.sink_max_side)
+    plan = V.var_block_mask_plan(p, st, w.qblock_side, rp, en, sink)
+    return (rp, en, sink, plan), (time.perf_counter() - t0) * 1e3
+
+
 # ----------------------------------------------------------------------------- CPU oracle arm
 
 def oracle_sample(inp, budget_s: float, seed: int = 0):
-    """Time the oracle on random query rows of the final step's dense attention,
-    sized to about budget_s: (TFLOP/s, seconds, rows, threads)."""
+    """Time the oracle on random query rows of the 1024px final step's dense
+    attention, sized to about budget_s: (TFLOP/s, seconds, rows, threads)."""
     import oracle
-    w = WORKLOADS[STEP_WORKLOAD]
+    w = WORKLOADS[W1024]
     q = inp.q[FINAL]
     B, H, N, D = q.shape
     L = cache_len(w.sides, FINAL)
@@ -337,21 +402,28 @@ def oracle_sample(inp, budget_s: float, seed: int = 0):
     return n_rows * 4.0 * L * D / dt / 1e12, dt, n_rows, oracle.num_threads()
 
 
-def step_config(inp):
-    w = WORKLOADS[STEP_WORKLOAD]
-    q = inp.q[FINAL]
-    B, H, N, D = q.shape
-    return {"workload": "final_step_1024px", "schedule": list(w.sides), "batch": B, "heads": H,
-            "head_dim": D, "queries": N, "keys": cache_len(w.sides, FINAL), "channels": w.channels,
-            "keep": f"{KEEP[0]}/{KEEP[1]}", "block_mask": f"qblock {QBLOCK}, radius {RADIUS}, sinks <= {SINK_SIDE}",
-            "rows": list(ROW_NAMES)}
+def step_config():
+    """The `config` of both arms' JSON lines."""
+    w, w2 = WORKLOADS[W1024], WORKLOADS[W2K]
+    return {"workload": "var_hot_path_step: 1024px final-scale dense + pruned 48x48 and 64x64 steps "
+                        "+ 2K final-scale block-sparse",
+            "batch": w.batch, "heads": w.heads, "head_dim": w.head_dim,
+            "dense": {"queries": w.sides[FINAL] ** 2, "keys": cache_len(w.sides, FINAL)},
+            "pruned": {"48x48": {"keep": "2/5", "keys": cache_len(w.sides, MID)},
+                       "64x64": {"keep": "1/5", "keys": cache_len(w.sides, FINAL)},
+                       "channels": w.channels},
+            "blocksparse": {"queries": w2.sides[-1] ** 2, "keys": cache_len(w2.sides, w2.steps[-1]),
+                            "mask": f"qblock {QBLOCK}, radius {RADIUS}, sinks <= {SINK_SIDE}"},
+            "rows": list(ROW_NAMES),
+            "l2": "inputs larger than L2 (1024px Q/K/V + hidden states 0.28 GB, 2K Q/K/V 0.83 GB per step)",
+            "per_gpu": "each rank runs the whole workload"}
 
 
 def run_reference(args):
     ws, rank, _ = dist_info()
     if rank != 0:
         return 0
-    inp = make_inputs(WORKLOADS[STEP_WORKLOAD], steps=(FINAL,))
+    inp = make_inputs(WORKLOADS[W1024], steps=(FINAL,))
     per_step = min(args.ref_seconds, 150.0 / (args.steps + args.warmup))
     vals = []
     for i in range(args.warmup + args.steps):
@@ -364,9 +436,9 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": step_config(inp),
+        "data": "synthetic", "config": step_config(),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
-                         "sample": f"{n_rows} random query rows of the final step's dense attention "
+                         "sample": f"{n_rows} random query rows of the 1024px final step's dense attention "
                                    "per step; throughput per FLOP"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -376,24 +448,47 @@ def run_reference(args):
 
 # ----------------------------------------------------------------------------- GPU arm
 
-def extra_rows(V, dev, step: Step, iters: int, peaks):
-    """Separate measurements: small kernels alone, the 2K block-sparse workload,
-    the 256px schedule."""
+def time_events(fn, n: int, stream) -> float:
+    """Mean ms of n back-to-back fn() on `stream` (CUDA events)."""
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n
+
+
+def extra_rows(V, dev, step: Step, inp, iters: int, peaks, host_bytes):
+    """Separate measurements: the small kernels alone, the fused pruned step, the
+    §8(f) rows, the tiny and 256px workloads, the host link ceiling."""
     rows = {}
     flush = L2Flush(dev)
-    calls = step.calls()
-    t = time_graph(calls[1], iters, flush)
-    rows["pivot_select_64x64_alone"] = {"ms": t, "GB/s": step.bytes_pivot / t / 1e6,
-                                        "frac_hbm": step.bytes_pivot / t / 1e6 / peaks["hbm_gbs"],
-                                        "timing": "CUDA graph replay after an L2 flush"}
-    t = time_graph(calls[3], iters, flush)
-    rows["restore_scatter_48to64_alone"] = {"ms": t, "GB/s": step.bytes_restore / t / 1e6,
-                                            "frac_hbm": step.bytes_restore / t / 1e6 / peaks["hbm_gbs"],
-                                            "timing": "CUDA graph replay after an L2 flush"}
-    # the pruned step with the outputs written in place (no compact buffer)
+    calls = dict(zip(ROW_NAMES, step.calls()))
+    for name in ("pivot_select_48", "pivot_select_64", "restore_scatter_40to48", "restore_scatter_48to64"):
+        t = time_graph(calls[name], iters, flush)
+        rows[name + "_alone"] = {"ms": t, "GB/s": step.bytes[name] / t / 1e6,
+                                 "frac_hbm": step.bytes[name] / t / 1e6 / peaks["hbm_gbs"],
+                                 "timing": "CUDA graph replay after an L2 flush"}
+    # the single-launch floor at the pivot's size: one copy of the 64x64 hidden states
+    xs = step.x[FINAL]
+    xd = torch.empty_like(xs)
+    t = time_graph(lambda: xd.copy_(xs), iters, flush)
+    rows["copy_floor_34MB_alone"] = {"ms": t, "GB/s": 2 * xs.numel() * 2 / t / 1e6,
+                                     "frac_hbm": 2 * xs.numel() * 2 / t / 1e6 / peaks["hbm_gbs"],
+                                     "note": "one torch copy_ launch of the 64x64 hidden states (read + write "
+                                             "2 x 33.6 MB): what a single launch of this size reaches",
+                                     "timing": "CUDA graph replay after an L2 flush"}
+    del xd
+    # the pruned 64x64 step with the outputs written in place (no compact buffer)
+    p, s = step.p, FINAL
+
     def fused():
-        step.V.var_attn_pruned_scatter(step.p, FINAL, step.q, step.k, step.v, step.idx, step.K, step.o_pruned)
-        step.V.var_restore_fill(step.p, FINAL, step.prev, step.idx, step.K, step.o_pruned)
+        V.var_attn_pruned_scatter(p, s, step.q[s], step.k, step.v, step.idx[s], step.K[s], step.out[s])
+        V.var_restore_fill(p, s, step.out[MID], step.idx[s], step.K[s], step.out[s])
 
     side = torch.cuda.Stream()
 
@@ -402,32 +497,31 @@ def extra_rows(V, dev, step: Step, iters: int, peaks):
         cur = torch.cuda.current_stream()
         side.wait_stream(cur)
         with torch.cuda.stream(side):
-            step.V.var_restore_fill(step.p, FINAL, step.prev, step.idx, step.K, step.o_pruned)
-        step.V.var_attn_pruned_scatter(step.p, FINAL, step.q, step.k, step.v, step.idx, step.K, step.o_pruned)
+            V.var_restore_fill(p, s, step.out[MID], step.idx[s], step.K[s], step.out[s])
+        V.var_attn_pruned_scatter(p, s, step.q[s], step.k, step.v, step.idx[s], step.K[s], step.out[s])
         cur.wait_stream(side)
 
     t = time_graph(fused, iters, flush)
     t_ov = time_graph(fused_overlapped, iters, flush)
-    t_chain = time_graph(lambda: (calls[2](), calls[3]()), iters, flush)
-    rows["pruned_attn_and_restore_fused"] = {"ms": t, "overlapped_ms": t_ov, "unfused_ms": t_chain,
-                                             "dense_equiv_TFLOP/s": step.flops_dense / t_ov / 1e9,
-                                             "timing": "CUDA graph replay after an L2 flush; overlapped = "
-                                                       "fill on a second stream beside the attention"}
+    t_chain = time_graph(lambda: (calls["attn_pruned_64"](), calls["restore_scatter_48to64"]()), iters, flush)
+    rows["pruned_64_attn_and_restore_fused"] = {
+        "ms": t, "overlapped_ms": t_ov, "unfused_ms": t_chain,
+        "timing": "CUDA graph replay after an L2 flush; overlapped = fill on a second stream beside the attention"}
     # attention-guided pivots (ARVAR): the 32x32 step's row statistics and saliency
     src = FINAL - 3
-    B, H, Ns, D = step.q_src.shape
-    o_src = torch.empty_like(step.q_src)
+    q_src = inp.q[src].to(dev)
+    B, H, Ns, D = q_src.shape
+    o_src = torch.empty_like(q_src)
     lse = torch.empty((B, H, Ns), dtype=torch.float32, device=dev)
     sal = torch.empty((B, H, Ns), dtype=torch.float32, device=dev)
-    gws = torch.empty(step.V.var_guided_pivot_workspace_bytes(step.p, FINAL), dtype=torch.uint8, device=dev)
-    gidx = torch.empty_like(step.idx)
-    t_plain = time_graph(lambda: step.V.var_attn_dense(step.p, src, step.q_src, step.k, step.v, o_src), iters, flush)
-    t_lse = time_graph(lambda: step.V.var_attn_dense_lse(step.p, src, step.q_src, step.k, step.v, o_src, lse),
+    gws = torch.empty(V.var_guided_pivot_workspace_bytes(p, FINAL), dtype=torch.uint8, device=dev)
+    gidx = torch.empty_like(step.idx[FINAL])
+    t_plain = time_graph(lambda: V.var_attn_dense(p, src, q_src, step.k, step.v, o_src), iters, flush)
+    t_lse = time_graph(lambda: V.var_attn_dense_lse(p, src, q_src, step.k, step.v, o_src, lse), iters, flush)
+    t_sal = time_graph(lambda: V.var_attn_saliency(p, src, q_src, step.k, lse, sal), iters, flush)
+    t_sel = time_graph(lambda: V.var_guided_pivot_select(p, FINAL, src, sal, step.K[FINAL], gidx, gws),
                        iters, flush)
-    t_sal = time_graph(lambda: step.V.var_attn_saliency(step.p, src, step.q_src, step.k, lse, sal), iters, flush)
-    t_sel = time_graph(lambda: step.V.var_guided_pivot_select(step.p, FINAL, src, sal, step.K, gidx, gws),
-                       iters, flush)
-    L_src = cache_len(WORKLOADS[STEP_WORKLOAD].sides, src)
+    L_src = cache_len(WORKLOADS[W1024].sides, src)
     fl_sal = 2.0 * B * H * Ns * Ns * D            # S^T = K_self Q^T
     rows["guided_pivot_from_32x32"] = {
         "ms": t_sal + t_sel, "saliency_ms": t_sal, "select_ms": t_sel,
@@ -437,91 +531,84 @@ def extra_rows(V, dev, step: Step, iters: int, peaks):
                 "statistics are written by the source step's own dense attention",
         "timing": "CUDA graph replay after an L2 flush"}
     # SparVAR dynamic pattern: the 32x32 step's block scores decide the 64x64 step's mask
-    d_sv, tau_sv = FINAL - 3, 0.8
-    U_sv, _ = step.V.var_sparvar_units(step.p, d_sv, SINK_SIDE)
-    sv_ws = torch.empty(step.V.var_sparvar_workspace_bytes(step.p, d_sv), dtype=torch.uint8, device=dev)
-    nqb_sv = (int(round(step.q_src.shape[2] ** 0.5)) // 8) ** 2
+    d_sv, tau_sv = src, 0.8
+    U_sv, _ = V.var_sparvar_units(p, d_sv, SINK_SIDE)
+    sv_ws = torch.empty(V.var_sparvar_workspace_bytes(p, d_sv), dtype=torch.uint8, device=dev)
+    nqb_sv = (int(round(Ns ** 0.5)) // 8) ** 2
     sv_sc = torch.empty((nqb_sv, U_sv), dtype=torch.float64, device=dev)
-    t_sc = time_graph(lambda: step.V.var_sparvar_scores(step.p, d_sv, SINK_SIDE, step.q_src, step.k, sv_ws, sv_sc),
-                      iters, flush)
+    t_sc = time_graph(lambda: V.var_sparvar_scores(p, d_sv, SINK_SIDE, q_src, step.k, sv_ws, sv_sc), iters, flush)
     t0 = time.perf_counter()
     A = sv_sc.cpu().numpy()
-    rp, en, sink = step.V.var_sparvar_mask_build(step.p, d_sv, FINAL, SINK_SIDE, A, tau_sv)
-    sv_plan = [torch.as_tensor(a, device=dev) for a in step.V.var_block_mask_plan(step.p, FINAL, QBLOCK, rp, en, sink)]
+    rp, en, sink = V.var_sparvar_mask_build(p, d_sv, FINAL, SINK_SIDE, A, tau_sv)
+    sv_plan = [torch.as_tensor(a, device=dev) for a in V.var_block_mask_plan(p, FINAL, QBLOCK, rp, en, sink)]
     t_host = (time.perf_counter() - t0) * 1e3
     sv_rp, sv_en = torch.as_tensor(rp, device=dev), torch.as_tensor(en, device=dev)
-    sv_mask = step.V.block_mask_struct(QBLOCK, sv_rp, sv_en, sink, sv_plan)
-    t_sv = time_graph(lambda: step.V.var_attn_blocksparse(step.p, FINAL, step.q, step.k, step.v, sv_mask,
-                                                           step.o_sparse), iters, flush)
-    pairs = mask_kept_pairs(WORKLOADS[STEP_WORKLOAD].sides, rp, en, sink, QBLOCK)
-    fl_sv = 4.0 * step.q.shape[0] * step.q.shape[1] * pairs * step.q.shape[3]
+    sv_mask = V.block_mask_struct(QBLOCK, sv_rp, sv_en, sink, sv_plan)
+    o_sv = torch.empty_like(step.q[FINAL])
+    t_sv = time_graph(lambda: V.var_attn_blocksparse(p, FINAL, step.q[FINAL], step.k, step.v, sv_mask, o_sv),
+                      iters, flush)
+    pairs = mask_kept_pairs(WORKLOADS[W1024].sides, rp, en, sink, QBLOCK)
+    fl_sv = 4.0 * B * H * pairs * D
     rows["sparvar_dynamic_mask_32_to_64"] = {
         "scores_ms": t_sc, "host_select_map_plan_ms": t_host, "attn_ms": t_sv,
-        "density": pairs / (step.N * step.L), "TFLOP/s": fl_sv / t_sv / 1e9,
-        "dense_equiv_TFLOP/s": step.flops_dense / t_sv / 1e9, "units": U_sv, "tau": tau_sv,
-        "note": "decision step 32x32: block scores (dense attention on unit-indicator values, "
-                f"{U_sv} units) -> host selection + index mapping -> block-sparse attention of the 64x64 step",
+        "density": pairs / (step.N[FINAL] * step.L[FINAL]), "TFLOP/s": fl_sv / t_sv / 1e9,
+        "effective_dense_equiv_TFLOP/s": step.flops["attn_dense_1024px"] / t_sv / 1e9, "units": U_sv, "tau": tau_sv,
+        "note": "decision step 32x32: block scores -> host selection + index mapping -> block-sparse "
+                "attention of the 64x64 step",
         "timing": "CUDA graph replay after an L2 flush; host part timed once"}
+    del q_src, o_src, o_sv
     # Branch Halving: the conditional half only, its rows repeated
-    t = time_graph(lambda: step.V.var_attn_dense_halved(step.p, FINAL, step.q, step.k, step.v, step.o_dense),
+    fd = step.flops["attn_dense_1024px"]
+    t = time_graph(lambda: V.var_attn_dense_halved(p, FINAL, step.q[FINAL], step.k, step.v, step.o_dense),
                    iters, flush)
-    rows["attn_dense_branch_halved"] = {"ms": t, "TFLOP/s": step.flops_dense / 2 / t / 1e9,
-                                        "frac_tensor": step.flops_dense / 2 / t / 1e9 / peaks["bf16_tflops"],
-                                        "dense_equiv_TFLOP/s": step.flops_dense / t / 1e9,
+    rows["attn_dense_branch_halved"] = {"ms": t, "TFLOP/s": fd / 2 / t / 1e9,
+                                        "frac_tensor": fd / 2 / t / 1e9 / peaks["bf16_tflops"],
+                                        "effective_dense_equiv_TFLOP/s": fd / t / 1e9,
                                         "timing": "CUDA graph replay after an L2 flush"}
-    # block-sparse attention on the 2K schedule (its own workload)
-    w = WORKLOADS["blocksparse_2k"]
-    st = w.steps[-1]
-    B, H, D = w.batch, w.heads, w.head_dim
-    p = V.problem(B, H, D, w.sides)
-    rp, en, sink = V.var_block_mask_build(p, st, w.qblock_side, w.radius, w.sink_max_side)
-    inp = make_inputs(w)
-    q, k, v = inp.q[st].to(dev), inp.k.to(dev), inp.v.to(dev)
-    del inp
-    o = torch.empty_like(q)
-    plan = [torch.as_tensor(a, device=dev) for a in V.var_block_mask_plan(p, st, w.qblock_side, rp, en, sink)]
-    m = V.block_mask_struct(w.qblock_side, torch.as_tensor(rp, device=dev), torch.as_tensor(en, device=dev), sink,
-                            plan)
-    stream = torch.cuda.current_stream(dev)
-
-    def bs():
-        V.var_attn_blocksparse(p, st, q, k, v, m, o, stream=stream)
-
-    for _ in range(3):
-        bs()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n = max(5, iters)
-    e0.record(stream)
-    for _ in range(n):
-        bs()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    t = e0.elapsed_time(e1) / n
-    N, L = q.shape[2], cache_len(w.sides, st)
-    pairs = mask_kept_pairs(w.sides, rp, en, sink, w.qblock_side)
-    fl = 4.0 * B * H * pairs * D
-    rows["attn_blocksparse_2k"] = {"ms": t, "TFLOP/s": fl / t / 1e9, "frac_tensor": fl / t / 1e9 / peaks["bf16_tflops"],
-                                   "dense_equiv_TFLOP/s": flops_attn(B, H, N, L, D) / t / 1e9,
-                                   "density": pairs / (N * L)}
-    del q, k, v, o
+    # the tiny workload: 256 queries against 680 keys, batch 1, head_dim 64 (launch-bound)
+    w = WORKLOADS["dense_tiny"]
+    inp_t = make_inputs(w)
+    st_t = w.steps[0]
+    pt = V.problem(w.batch, w.heads, w.head_dim, w.sides)
+    qt, kt, vt = inp_t.q[st_t].to(dev), inp_t.k.to(dev), inp_t.v.to(dev)
+    ot = torch.empty_like(qt)
+    t = time_graph(lambda: V.var_attn_dense(pt, st_t, qt, kt, vt, ot), iters, flush)
+    fl = flops_attn(w.batch, w.heads, w.sides[st_t] ** 2, cache_len(w.sides, st_t), w.head_dim)
+    rows["dense_tiny_256q_680k"] = {"ms": t, "TFLOP/s": fl / t / 1e9, "launches": 1,
+                                    "note": "launch-bound: 0.71 GFLOP on 16 CTAs",
+                                    "timing": "CUDA graph replay after an L2 flush"}
     # the whole 256px schedule, dense (launch-bound)
     w = WORKLOADS["dense_256px"]
-    inp = make_inputs(w)
-    B, H, D = w.batch, w.heads, w.head_dim
-    p = V.problem(B, H, D, w.sides)
-    k, v = inp.k.to(dev), inp.v.to(dev)
-    qs = {s: inp.q[s].to(dev) for s in w.steps}
-    os_ = {s: torch.empty_like(qs[s]) for s in w.steps}
+    inp_s = make_inputs(w)
+    B2, H2, D2 = w.batch, w.heads, w.head_dim
+    ps = V.problem(B2, H2, D2, w.sides)
+    ks, vs = inp_s.k.to(dev), inp_s.v.to(dev)
+    qs = {s2: inp_s.q[s2].to(dev) for s2 in w.steps}
+    os_ = {s2: torch.empty_like(qs[s2]) for s2 in w.steps}
 
     def sched():
-        for s in w.steps:
-            V.var_attn_dense(p, s, qs[s], k, v, os_[s])
+        for s2 in w.steps:
+            V.var_attn_dense(ps, s2, qs[s2], ks, vs, os_[s2])
 
     t = time_graph(sched, iters, flush)
-    fl = sum(flops_attn(B, H, w.sides[s] ** 2, cache_len(w.sides, s), D) for s in w.steps)
+    fl = sum(flops_attn(B2, H2, w.sides[s2] ** 2, cache_len(w.sides, s2), D2) for s2 in w.steps)
+    t_last = time_graph(lambda: V.var_attn_dense(ps, w.steps[-1], qs[w.steps[-1]], ks, vs, os_[w.steps[-1]]),
+                        iters, flush)
     rows["schedule_256px_dense_10_steps"] = {"ms": t, "TFLOP/s": fl / t / 1e9, "launches": len(w.steps),
+                                             "final_step_ms": t_last,
                                              "timing": "CUDA graph replay after an L2 flush"}
+    # the host link: one pinned copy of the e2e leg's upload and download sizes
+    h_in, h_out = host_bytes
+    hb = torch.empty(h_in, dtype=torch.uint8).pin_memory()
+    db = torch.empty(h_in, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    t_h2d = time_events(lambda: db.copy_(hb, non_blocking=True), 3, stream)
+    t_d2h = time_events(lambda: hb[:h_out].copy_(db[:h_out], non_blocking=True), 3, stream)
+    rows["host_link_ceiling"] = {"h2d_GB/s": h_in / t_h2d / 1e6, "h2d_ms": t_h2d, "h2d_bytes": h_in,
+                                 "d2h_GB/s": h_out / t_d2h / 1e6, "d2h_ms": t_d2h, "d2h_bytes": h_out,
+                                 "note": "one cudaMemcpyAsync from/to pinned host memory of the e2e leg's "
+                                         "per-step upload and download sizes"}
+    del hb, db
     return rows
 
 
@@ -534,11 +621,13 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     import visual_autoregressive_next_var_b300 as V
 
-    inp = make_inputs(WORKLOADS[STEP_WORKLOAD], steps=(FINAL - 3, FINAL - 1, FINAL))
-    step = Step(V, dev, inp)
+    inp = make_inputs(WORKLOADS[W1024], steps=(FINAL - 3, PREV, MID, FINAL))
+    inp2k = make_inputs(WORKLOADS[W2K])
+    mask2k, mask_ms = build_mask_2k(V)
+    step = Step(V, dev, inp, inp2k, mask2k)
     stream = torch.cuda.current_stream(dev)
-    flops_equiv = 3.0 * step.flops_dense
-    flops_exec = step.flops_dense + step.flops_pruned + step.flops_sparse
+    flops_step = sum(step.flops.values())
+    flops_equiv = sum(step.flops_dense_equiv.values())
 
     for _ in range(args.warmup):
         step.run(stream)
@@ -557,79 +646,68 @@ def run_gpu(args):
     if st != 0:
         raise RuntimeError(f"device status {st} ({V.var_status_string(st)})")
     peaks = load_peaks()
-    value = ws * flops_equiv / ms_max / 1e9
+    value = ws * flops_step / ms_max / 1e9
 
     # per-row figures inside the timed region
-    row_flops = {"attn_dense": step.flops_dense, "attn_pruned": step.flops_pruned,
-                 "attn_blocksparse": step.flops_sparse}
-    row_bytes = {"pivot_select": step.bytes_pivot, "restore_scatter": step.bytes_restore}
     rows = {}
     for name, t in zip(ROW_NAMES, per_row):
-        r = {"ms": t}
-        if name in row_flops:
-            r["TFLOP/s"] = row_flops[name] / t / 1e9
+        r = {"ms": t, "kernel": KERNEL_NAMES[name]}
+        if name in step.flops:
+            r["TFLOP/s"] = step.flops[name] / t / 1e9
             r["frac_tensor"] = r["TFLOP/s"] / peaks["bf16_tflops"]
-            r["dense_equiv_TFLOP/s"] = step.flops_dense / t / 1e9
+            r["effective_dense_equiv_TFLOP/s"] = step.flops_dense_equiv[name] / t / 1e9
         else:
-            r["GB/s"] = row_bytes[name] / t / 1e6
+            r["GB/s"] = step.bytes[name] / t / 1e6
             r["frac_hbm"] = r["GB/s"] / peaks["hbm_gbs"]
         rows[name] = r
-    rows["attn_blocksparse"]["density"] = step.sparse_pairs / (step.N * step.L)
-    rows["block_mask_build_and_plan_host_once"] = {"ms": step.mask_build_ms}
+    rows["attn_blocksparse_2k"]["density"] = step.sparse_pairs / (step.N2 * step.L2)
+    rows["block_mask_build_and_plan_2k_host_once"] = {"ms": mask_ms}
     dom = max(range(len(ROW_NAMES)), key=lambda i: per_row[i])
     dom_name = ROW_NAMES[dom]
-    kernel_names = {"attn_dense": "attn_kernel<128, dense>", "attn_pruned": "attn_kernel<128, gather>",
-                    "attn_blocksparse": "attn_kernel<128, sparse>", "pivot_select": "pivot kernels",
-                    "restore_scatter": "restore_scatter_kernel<128>"}
-    if dom_name in row_flops:
-        achieved = row_flops[dom_name] / per_row[dom] / 1e9
-        roof = {"kernel": kernel_names[dom_name], "bound": "tensor", "achieved": achieved,
+    if dom_name in step.flops:
+        achieved = step.flops[dom_name] / per_row[dom] / 1e9
+        roof = {"kernel": KERNEL_NAMES[dom_name], "row": dom_name, "bound": "tensor", "achieved": achieved,
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
                 "peak_source": f"{peaks['source']} dense bf16 burst (cuBLAS)",
-                "traffic": ncu_traffic(f"{kernel_names[dom_name]}:final_step_1024px"),
-                "algorithmic_flops_per_launch": row_flops[dom_name],
-                "launch_ms": per_row[dom]}
+                "traffic": ncu_traffic(TRAFFIC_KEYS[dom_name]) if dom_name in TRAFFIC_KEYS else None,
+                "algorithmic_flops_per_launch": step.flops[dom_name], "launch_ms": per_row[dom]}
     else:
-        achieved = row_bytes[dom_name] / per_row[dom] / 1e6
-        roof = {"kernel": kernel_names[dom_name], "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "peak_source": f"{peaks['source']} copy",
-                "traffic": ncu_traffic(f"{kernel_names[dom_name]}:final_step_1024px"),
-                "algorithmic_bytes_per_launch": row_bytes[dom_name], "launch_ms": per_row[dom]}
+        achieved = step.bytes[dom_name] / per_row[dom] / 1e6
+        roof = {"kernel": KERNEL_NAMES[dom_name], "row": dom_name, "bound": "hbm", "achieved": achieved,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "peak_source": f"{peaks['source']} copy", "traffic": None,
+                "algorithmic_bytes_per_launch": step.bytes[dom_name], "launch_ms": per_row[dom]}
 
     # end to end through the public API with host buffers: every step uploads its
-    # inputs (Q, the whole K/V cache, X, the previous step's output) from pinned
-    # host memory and downloads its results.  Pipelined over two device buffer
-    # sets and three streams, as a run of steps would be: step i+1's upload and
-    # step i-1's download overlap step i's kernels.  The serial order (upload,
-    # kernels, download, one stream) is reported beside it.
-    host = {"q": inp.q[FINAL].pin_memory(), "k": inp.k.pin_memory(), "v": inp.v.pin_memory(),
-            "x": inp.x[FINAL].pin_memory(), "prev": step.prev.cpu().pin_memory()}
-    outs = [{"o_dense": torch.empty(step.o_dense.shape, dtype=torch.bfloat16).pin_memory(),
-             "idx": torch.empty(step.idx.shape, dtype=torch.int32).pin_memory(),
-             "o_pruned": torch.empty(step.o_pruned.shape, dtype=torch.bfloat16).pin_memory(),
-             "o_sparse": torch.empty(step.o_sparse.shape, dtype=torch.bfloat16).pin_memory()} for _ in range(2)]
+    # inputs (the 1024px Q's, K/V cache and hidden states, the 40x40 output, the
+    # 2K Q and K/V cache) from pinned host memory and downloads its results.
+    # Pipelined over two device buffer sets and three streams, as a run of steps
+    # would be: step i+1's upload and step i-1's download overlap step i's
+    # kernels.  The serial order (upload, kernels, download, one stream) is
+    # reported beside it.
+    host = {"q64": inp.q[FINAL].pin_memory(), "q48": inp.q[MID].pin_memory(), "k": inp.k.pin_memory(),
+            "v": inp.v.pin_memory(), "x48": inp.x[MID].pin_memory(), "x64": inp.x[FINAL].pin_memory(),
+            "prev40": step.prev.cpu().pin_memory(), "q2k": inp2k.q[step.st2].pin_memory(),
+            "k2k": inp2k.k.pin_memory(), "v2k": inp2k.v.pin_memory()}
+    outs = [{k: torch.empty(t.shape, dtype=t.dtype).pin_memory() for k, t in step.results().items()}
+            for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in outs[0].values())
-    sets = [step, Step(V, dev, inp)]
+    sets = [step, Step(V, dev, inp, inp2k, mask2k)]
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_out = [torch.cuda.Event() for _ in range(2)]
 
     def upload(st, strm):
         with torch.cuda.stream(strm):
-            st.q.copy_(host["q"], non_blocking=True)
-            st.k.copy_(host["k"], non_blocking=True)
-            st.v.copy_(host["v"], non_blocking=True)
-            st.x.copy_(host["x"], non_blocking=True)
-            st.prev.copy_(host["prev"], non_blocking=True)
+            for d, h in st.uploads(host):
+                d.copy_(h, non_blocking=True)
 
     def download(st, o, strm):
         with torch.cuda.stream(strm):
-            o["o_dense"].copy_(st.o_dense, non_blocking=True)
-            o["idx"].copy_(st.idx, non_blocking=True)
-            o["o_pruned"].copy_(st.o_pruned, non_blocking=True)
-            o["o_sparse"].copy_(st.o_sparse, non_blocking=True)
+            for k, t in st.results().items():
+                o[k].copy_(t, non_blocking=True)
 
     def e2e_serial():
         upload(step, stream)
@@ -677,18 +755,18 @@ def run_gpu(args):
     ms_e2e = reduce_max(e0.elapsed_time(e1) / e2e_steps, ws, dev)
     del sets[1]
 
-    cfg = step_config(inp)
-    cfg["l2"] = "inputs larger than L2 (Q/K/V 206 MB + X 34 MB per step)"
-    cfg["per_gpu"] = "each rank runs the whole workload"
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
-        "value_note": "dense-equivalent: 3 x the final-scale dense attention FLOPs per step "
-                      f"({flops_equiv / 1e9:.1f} GFLOP); executed algorithmic FLOPs "
-                      f"{flops_exec / 1e9:.1f} GFLOP -> {ws * flops_exec / ms_max / 1e9:.1f} TFLOP/s",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": step_config(),
+        "value_note": f"algorithmic: {flops_step / 1e9:.1f} GFLOP executed per step (4 D per computed "
+                      "(query, key) pair); the dense-equivalent effective figure "
+                      f"({flops_equiv / 1e9:.1f} GFLOP: every attention variant counted as full dense "
+                      f"attention) is {ws * flops_equiv / ms_max / 1e9:.1f} TFLOP/s and is not a fraction "
+                      "of any peak",
+        "effective_dense_equiv_TFLOP/s": ws * flops_equiv / ms_max / 1e9,
         "roofline": roof,
-        "e2e": {"value": ws * flops_equiv / ms_e2e / 1e9, "unit": "TFLOP/s", "ms_per_step": ms_e2e,
+        "e2e": {"value": ws * flops_step / ms_e2e / 1e9, "unit": "TFLOP/s", "ms_per_step": ms_e2e,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "mode": f"pipelined over {e2e_steps} steps: upload of step i+1 and download of step i-1 "
                         "overlap step i's kernels (two device buffer sets, three streams)",
@@ -698,13 +776,12 @@ def run_gpu(args):
         "rows": rows,
     }
     if not args.no_rows:
-        line["rows"].update(extra_rows(V, dev, step, max(5, min(args.steps, 20)), peaks))
+        line["rows"].update(extra_rows(V, dev, step, inp, max(5, min(args.steps, 20)), peaks, (h2d, d2h)))
     if rank == 0 and ws == 1 and not args.no_cpu:
         tf, dt, n_rows, thr = oracle_sample(inp, args.cpu_seconds)
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
-                                "sample": f"{n_rows} random query rows of the final step's dense attention "
-                                          f"(of {step.q.shape[0] * step.q.shape[1] * step.N}), {dt:.1f} s; "
-                                          "throughput per FLOP"}
+                                "sample": f"{n_rows} random query rows of the 1024px final step's dense attention "
+                                          f"(of {2 * 16 * step.N[FINAL]}), {dt:.1f} s; throughput per FLOP"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:

@@ -21,8 +21,11 @@
  *    var_device_status().
  *  - Return value: a var_status code.  Arguments are checked on the host before
  *    any launch; a failing check launches nothing.  Faults detected on the
- *    device (a pipeline wait that timed out) are recorded in a device status
- *    word read by var_device_status().
+ *    device (a pipeline wait that timed out, a malformed block mask, an input
+ *    outside the exactly handled range) are recorded in the call's status
+ *    word: the caller's own device word named by var_problem.status, read with
+ *    var_check_status(), or, when that is NULL, the library's per-device word
+ *    read with var_device_status().
  *  - No C++ exception crosses this interface.
  */
 #ifndef VARATTN_H
@@ -62,6 +65,12 @@ typedef struct {
     int32_t side[VAR_MAX_SCALES]; /* s_1..s_n: side lengths of the token grids */
     int32_t kv_capacity;  /* rows per (b,h) in the K/V buffers; 0 = exactly L(step) */
     float softmax_scale;  /* 0 = 1/sqrt(head_dim) */
+    /* Optional DEVICE pointer to a caller-owned int32 status word (4-byte
+     * aligned, zero before the first call).  The kernels of every call made
+     * with this problem record there the first fault they detect (compare-and-
+     * swap from 0), so a fault is tied to the calls that share the word, not
+     * to the device.  NULL: the library's per-device word (var_device_status). */
+    int32_t* status;
 } var_problem;
 
 /*
@@ -84,10 +93,13 @@ VAR_API int var_attn_dense(const var_problem* p, int32_t step, const void* q, co
 VAR_API size_t var_pivot_workspace_bytes(const var_problem* p, int32_t step, int32_t channels);
 
 /*
- * Device workspace bytes the path's calls need at `step` with `channels` hidden
- * channels and keep_k kept queries: pivot selection is the only one that takes
- * scratch, so this is var_pivot_workspace_bytes (0 for invalid arguments,
- * keep_k outside [0, N] included).
+ * Device workspace bytes the dense -> pivot -> pruned -> restore path needs at
+ * `step` with `channels` hidden channels and keep_k kept queries.  Of those
+ * calls only pivot selection takes scratch, so this equals
+ * var_pivot_workspace_bytes; keep_k is checked (0 for keep_k outside [0, N] or
+ * other invalid arguments) but does not change the size.  The attention-guided
+ * pivots and the dynamic sparse pattern size their own scratch with
+ * var_guided_pivot_workspace_bytes and var_sparvar_workspace_bytes.
  */
 VAR_API size_t var_workspace_bytes(const var_problem* p, int32_t step, int32_t channels, int32_t keep_k);
 
@@ -103,8 +115,8 @@ VAR_API size_t var_workspace_bytes(const var_problem* p, int32_t step, int32_t c
  * as a pairwise-halving tree over channels): fp32 scores with a certified
  * error bound decide every token outside a narrow band around the K-th score;
  * band tokens are decided by count or re-scored in fp64 on the device.
- * Two kernels on `stream`, the second launched as a programmatic dependent of
- * the first.
+ * Three kernels on `stream`: the channel sums, then the scores and the
+ * selection, each launched as a programmatic dependent of its predecessor.
  * x: [B][N][channels] bf16, channels a positive multiple of 32, |x| < 2^20.
  * idx: [B][keep_k] int32 (device).  scores: optional [B][N] fp32 (device) or NULL.
  * workspace: device memory of var_pivot_workspace_bytes() bytes, 256-byte
@@ -131,10 +143,11 @@ VAR_API int var_pivot_select(const var_problem* p, int32_t step, const void* x, 
  * device, with that device current); make that first call before any stream
  * capture.  All calls share the one array and it keeps the last call's
  * contents (nothing in it needs clearing: each call writes every word it
- * reads, and resets its own completion counters): calls whose work overlaps
- * on the GPU -- on different streams, or from different host threads -- race
- * and must be serialised by the caller.
- * Arguments, results and other errors are those of var_pivot_select.
+ * reads before reading it): calls whose work overlaps on the GPU -- on
+ * different streams, or from different host threads -- race and must be
+ * serialised by the caller.
+ * Arguments, results and other errors are those of var_pivot_select (the same
+ * checks, in the same order), then VAR_ERR_WORKSPACE beyond the array's limits.
  */
 VAR_API int var_pivot_select_noalloc(const var_problem* p, int32_t step, const void* x,
                                      int32_t channels, int32_t keep_k, int32_t* idx,
@@ -401,12 +414,13 @@ VAR_API int var_sparvar_mask_build(const var_problem* p, int32_t decision_step, 
 /*
  * Diagnostics: launch a one-thread kernel whose bounded wait on a barrier that
  * nothing arrives on gives up after limit_us microseconds (1 .. 10^7) and
- * records VAR_ERR_TIMEOUT in the device status word, exactly as a pipeline
- * wait of the kernels above that gave up would.  It lets a caller check the
- * failure path (var_device_status) without a fault: the device stays usable.
- * Asynchronous on `stream`.  Errors: VAR_ERR_INVALID_ARG, VAR_ERR_CUDA.
+ * records VAR_ERR_TIMEOUT in `status` (a device status word as in var_problem;
+ * NULL = the per-device word), exactly as a pipeline wait of the kernels above
+ * that gave up would.  It lets a caller check the failure path
+ * (var_check_status, var_device_status) without a fault: the device stays
+ * usable.  Asynchronous on `stream`.  Errors: VAR_ERR_INVALID_ARG, VAR_ERR_CUDA.
  */
-VAR_API int var_selftest_wait_timeout(int32_t limit_us, void* stream);
+VAR_API int var_selftest_wait_timeout(int32_t limit_us, int32_t* status, void* stream);
 
 /* floor(n * num / den) in exact integer arithmetic (the kept-query count). */
 VAR_API int32_t var_keep_count(int32_t n, int32_t num, int32_t den);
@@ -415,11 +429,24 @@ VAR_API int32_t var_keep_count(int32_t n, int32_t num, int32_t den);
 VAR_API const char* var_status_string(int status);
 
 /*
- * Read (and optionally clear) the device status word of the current device:
- * VAR_OK, or the first VAR_ERR_TIMEOUT / VAR_ERR_NUMERIC a kernel recorded.
- * Synchronises the device.  Returns VAR_OK or VAR_ERR_CUDA.
+ * Read (and optionally clear) the library's per-device status word of the
+ * current device -- the word of calls whose var_problem.status is NULL:
+ * VAR_OK, or the first fault code a kernel recorded.  Synchronises the device.
+ * Returns VAR_OK, VAR_ERR_INVALID_ARG (status_out NULL) or VAR_ERR_CUDA.
  */
 VAR_API int var_device_status(int32_t* status_out, int32_t clear);
+
+/*
+ * Read (and optionally clear) a caller-owned device status word (see
+ * var_problem.status; NULL = the per-device word) in stream order: the read
+ * follows the work already queued on `stream`, and only `stream` is
+ * synchronised.  *status_out = VAR_OK or the first fault code recorded there
+ * (VAR_ERR_TIMEOUT, VAR_ERR_INVALID_ARG for a malformed block mask,
+ * VAR_ERR_UNSUPPORTED for a mask beyond the kernel's limits, VAR_ERR_NUMERIC).
+ * Returns VAR_OK, VAR_ERR_INVALID_ARG (status_out NULL, misaligned word) or
+ * VAR_ERR_CUDA.
+ */
+VAR_API int var_check_status(const int32_t* status, int32_t* status_out, int32_t clear, void* stream);
 
 #ifdef __cplusplus
 }

@@ -32,3 +32,9 @@ def check_device_status():
     import visual_autoregressive_next_var_b300 as V
     st = V.var_device_status(clear=True)
     assert st == 0, f"device status word: {st} ({V.var_status_string(st)})"
+
+
+def to_bf16(a: np.ndarray) -> torch.Tensor:
+    """The oracle's own fp64 result stored as bf16 (round to nearest even through
+    fp32), for chained stages whose next input is a stored bf16 tensor."""
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float64)).float().to(torch.bfloat16)

@@ -248,8 +248,8 @@ def test_sparvar_rejects_bad_arguments():
 
 def test_selftest_wait_timeout_rejects_bad_limits():
     L = V.lib()
-    assert L.var_selftest_wait_timeout(0, None) == V.VAR_ERR_INVALID_ARG
-    assert L.var_selftest_wait_timeout(10000001, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_selftest_wait_timeout(0, None, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_selftest_wait_timeout(10000001, None, None) == V.VAR_ERR_INVALID_ARG
 
 
 def test_workspace_bytes_is_the_pivot_scratch():
@@ -257,3 +257,53 @@ def test_workspace_bytes_is_the_pivot_scratch():
     assert V.var_workspace_bytes(p, 12, 2048, 819) == V.var_pivot_workspace_bytes(p, 12, 2048) > 0
     assert V.var_workspace_bytes(p, 12, 2048, 4097) == 0       # keep_k above N
     assert V.var_workspace_bytes(p, 12, 2048, -1) == 0
+
+
+def test_noalloc_pivot_rejects_what_the_workspace_version_rejects():
+    """var_pivot_select_noalloc runs the same argument checks, in the same order,
+    as var_pivot_select; only then come the limits of its static scratch."""
+    L = V.lib()
+    f = _fake()
+    good = dict(b=2, h=16, d=128, sides=SCHEDULE_1024, cap=0, scale=0.0)
+    cases = [
+        (dict(), 12, f, 2048, 819, f),                      # valid: both fail only later (workspace / device)
+        (dict(d=96), 12, f, 2048, 819, f),                  # head_dim
+        (dict(h=0), 12, f, 2048, 819, f),                   # heads
+        (dict(), 13, f, 2048, 819, f),                      # step past the schedule
+        (dict(), -1, f, 2048, 819, f),
+        (dict(cap=100), 12, f, 2048, 819, f),               # kv_capacity < L
+        (dict(scale=-1.0), 12, f, 2048, 819, f),            # softmax scale
+        (dict(), 12, None, 2048, 819, f),                   # null x
+        (dict(), 12, f, 2040, 819, f),                      # channels not a multiple of 32
+        (dict(), 12, f, 0, 819, f),
+        (dict(), 12, f, 2048, 4097, f),                     # keep_k > N
+        (dict(), 12, f, 2048, -1, f),
+        (dict(), 12, f, 2048, 819, None),                   # idx null with keep_k > 0
+        (dict(), 12, C.c_void_p(0x10008), 2048, 819, f),    # misaligned x
+    ]
+    for over, step, x, ch, k, idx in cases[1:]:
+        a = dict(good, **over)
+        p = V.problem(a["b"], a["h"], a["d"], a["sides"], kv_capacity=a["cap"], softmax_scale=a["scale"])
+        ws = L.var_pivot_workspace_bytes(C.byref(V.problem(2, 16, 128, SCHEDULE_1024)), 12, 2048)
+        want = L.var_pivot_select(C.byref(p), step, x, ch, k, idx, None, f, ws, None)
+        got = L.var_pivot_select_noalloc(C.byref(p), step, x, ch, k, idx, None, None)
+        assert want not in (V.VAR_OK, V.VAR_ERR_WORKSPACE, V.VAR_ERR_CUDA), (over, step, ch, k, want)
+        assert got == want, (over, step, ch, k, got, want)
+    # beyond the static scratch: batch 8, channels 8192 -- after the common checks pass
+    p8 = V.problem(8, 1, 128, (1, 16))
+    assert L.var_pivot_select_noalloc(C.byref(p8), 1, f, 64, 4, f, None, None) == V.VAR_ERR_WORKSPACE
+    p1 = V.problem(1, 1, 128, (1, 16))
+    assert L.var_pivot_select_noalloc(C.byref(p1), 1, f, 8192, 4, f, None, None) == V.VAR_ERR_WORKSPACE
+    assert L.var_pivot_select_noalloc(C.byref(p1), 1, f, 8192, 4, None, None, None) == V.VAR_ERR_INVALID_ARG
+
+
+def test_status_word_must_be_aligned():
+    L = V.lib()
+    f = _fake()
+    p = V.problem(1, 2, 64, SCHEDULE_256)
+    p.status = 0x10002
+    assert L.var_attn_dense(C.byref(p), 9, f, f, f, f, None) == V.VAR_ERR_INVALID_ARG
+    out = C.c_int32()
+    assert L.var_check_status(C.c_void_p(0x10002), C.byref(out), 0, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_check_status(f, None, 0, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_selftest_wait_timeout(100, C.c_void_p(0x10002), None) == V.VAR_ERR_INVALID_ARG

@@ -91,7 +91,7 @@ def test_blocksparse_covering_window_equals_dense():
     check_device_status()
 
 
-def test_blocksparse_2k_sampled_and_deterministic():
+def test_blocksparse_2k_sampled_two_whole_heads_and_deterministic():
     w = WORKLOADS["blocksparse_2k"]
     inp = make_inputs(w)
     step = w.steps[0]
@@ -112,6 +112,12 @@ def test_blocksparse_2k_sampled_and_deterministic():
                            mask=oracle.mask_spec(w.sides, step, w.qblock_side, w.radius, w.sink_max_side))
     got = o1.reshape(-1, D)[torch.as_tensor(rows, device=DEV)]
     assert_close(got, ref, "blocksparse 2k sampled")
+    # every row of two whole (b, h): the first and the last
+    spec = oracle.mask_spec(w.sides, step, w.qblock_side, w.radius, w.sink_max_side)
+    for bh in (0, B * H - 1):
+        rows = np.arange(bh * N, (bh + 1) * N, dtype=np.int64)
+        ref = oracle.attention(q, inp.k, inp.v, L, rows=rows, mask=spec)
+        assert_close(o1.reshape(-1, D)[bh * N:(bh + 1) * N], ref, f"blocksparse 2k (b,h) {bh} every row")
     check_device_status()
 
 

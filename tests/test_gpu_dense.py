@@ -66,7 +66,9 @@ def test_dense_256px_every_step_on_one_cache():
     check_device_status()
 
 
-def test_dense_1024px_sampled_rows_and_determinism():
+def test_dense_1024px_every_row_and_determinism():
+    """The 1024px final step (2 x 16 x 4,096 queries against 10,521 keys), every
+    output row against the oracle, and two runs bit for bit."""
     w = WORKLOADS["dense_1024px"]
     inp = make_inputs(w)
     step = w.steps[0]
@@ -80,11 +82,7 @@ def test_dense_1024px_sampled_rows_and_determinism():
     V.var_attn_dense(p, step, qd, kd, vd, o2)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2), "two runs on the same inputs differ"
-    B, H, N, D = q.shape
-    rows = sample_rows(B, H, N, 160, seed=5)
-    ref = oracle.attention(q, inp.k, inp.v, L, rows=rows)
-    got = o1.reshape(-1, D)[torch.as_tensor(rows, device=DEV)]
-    assert_close(got, ref, "dense_1024px sampled")
+    assert_close(o1, oracle.attention(q, inp.k, inp.v, L), "dense_1024px every row")
     check_device_status()
 
 

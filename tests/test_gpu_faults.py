@@ -16,7 +16,7 @@ DEV = "cuda"
 
 def test_wait_that_runs_out_is_reported_and_the_device_stays_usable():
     V.var_device_status(clear=True)
-    V.var_selftest_wait_timeout(20000)                # 20 ms
+    V.var_selftest_wait_timeout(20000)                # 20 ms, the per-device word
     torch.cuda.synchronize()
     assert V.var_device_status(clear=True) == V.VAR_ERR_TIMEOUT
     assert V.var_device_status(clear=False) == 0      # cleared

@@ -7,7 +7,7 @@ import torch
 import oracle
 import visual_autoregressive_next_var_b300 as V
 from var_synth import WORKLOADS, cache_len, make_inputs, randn_bf16
-from tests._util import assert_close, check_device_status, sample_rows
+from tests._util import assert_close, check_device_status, sample_rows, to_bf16
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -128,7 +128,8 @@ def test_fused_pruned_step_equals_chain(fill_first):
     ws = torch.empty(V.var_pivot_workspace_bytes(p, step, x.shape[2]), dtype=torch.uint8, device=DEV)
     idx = torch.empty((B, K), dtype=torch.int32, device=DEV)
     V.var_pivot_select(p, step, x, K, idx, ws)
-    prev = randn_bf16((B, H, 48 * 48, D), 77).to(DEV)
+    prev_c = randn_bf16((B, H, 48 * 48, D), 77)
+    prev = prev_c.to(DEV)
     oc = torch.empty((B, H, K, D), dtype=torch.bfloat16, device=DEV)
     chain = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=DEV)
     V.var_attn_pruned(p, step, qd, kd, vd, idx, K, oc)
@@ -142,11 +143,14 @@ def test_fused_pruned_step_equals_chain(fill_first):
         V.var_restore_fill(p, step, prev, idx, K, fused)
     torch.cuda.synchronize()
     assert torch.equal(fused, chain)
-    # and against the oracle on sampled kept and upsampled rows
-    ref = oracle.restore_scatter(prev.cpu(), oc.cpu(), idx.cpu().numpy(), 64)
-    rows = sample_rows(B, H, N, 200, seed=3)
-    got = fused.reshape(-1, D)[torch.as_tensor(rows, device=DEV)]
-    assert_close(got, ref.reshape(-1, D)[rows], "fused step")
+    # against the oracle's own step: its pivots (equal to the GPU's, bit for
+    # bit), its pruned rows stored as bf16, and its restore of the synthetic prev
+    ref_idx, _ = oracle.pivot_select(inp.x[step], K)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    qrows = (np.arange(B * H)[:, None] * N + ref_idx[np.arange(B * H) // H]).reshape(-1)
+    oc_ref = to_bf16(oracle.attention(q, inp.k, inp.v, L, rows=qrows)).reshape(B, H, K, D)
+    ref = oracle.restore_scatter(prev_c, oc_ref, ref_idx, 64)
+    assert_close(fused, ref, "fused step, every row")
     check_device_status()
 
 
@@ -155,13 +159,13 @@ def test_fused_pruned_step_head_dim_64_ragged():
     sides, D, B, H = (1, 2, 4, 6, 9, 14, 20, 23), 64, 2, 3
     step = len(sides) - 1
     L, N = cache_len(sides, step), sides[step] ** 2
-    q = randn_bf16((B, H, N, D), 91).to(DEV)
-    k = randn_bf16((B, H, L, D), 92).to(DEV)
-    v = randn_bf16((B, H, L, D), 93).to(DEV)
-    prev = randn_bf16((B, H, 20 * 20, D), 94).to(DEV)
+    qc, kc, vc = randn_bf16((B, H, N, D), 91), randn_bf16((B, H, L, D), 92), randn_bf16((B, H, L, D), 93)
+    prev_c = randn_bf16((B, H, 20 * 20, D), 94)
+    q, k, v, prev = qc.to(DEV), kc.to(DEV), vc.to(DEV), prev_c.to(DEV)
     K = 101
     g = torch.Generator().manual_seed(95)
-    idx = torch.stack([torch.sort(torch.randperm(N, generator=g)[:K])[0] for _ in range(B)]).to(torch.int32).to(DEV)
+    idx_c = torch.stack([torch.sort(torch.randperm(N, generator=g)[:K])[0] for _ in range(B)]).to(torch.int32)
+    idx = idx_c.to(DEV)
     p = V.problem(B, H, D, sides)
     oc = torch.empty((B, H, K, D), dtype=torch.bfloat16, device=DEV)
     chain = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=DEV)
@@ -172,6 +176,13 @@ def test_fused_pruned_step_head_dim_64_ragged():
     V.var_restore_fill(p, step, prev, idx, K, fused)
     torch.cuda.synchronize()
     assert torch.equal(fused, chain)
+    # every row against the oracle: kept rows are attention rows, the rest the upsample
+    ic = idx_c.numpy()
+    qrows = (np.arange(B * H)[:, None] * N + ic[np.arange(B * H) // H]).reshape(-1)
+    oc_ref = oracle.attention(qc, kc, vc, L, rows=qrows)
+    assert_close(oc.reshape(-1, D), oc_ref, "pruned rows, head_dim 64")
+    ref = oracle.restore_scatter(prev_c, to_bf16(oc_ref).reshape(B, H, K, D), ic, sides[step])
+    assert_close(fused, ref, "fused step head_dim 64, every row")
     check_device_status()
 
 
@@ -246,8 +257,9 @@ def test_restore_scatter(sp, s, K, D):
 
 def test_pruned_chain_1024px():
     """40x40 dense -> 48x48 pruned (r=0.4) + restore -> 64x64 pruned (r=0.2) + restore.
-    The oracle runs the same chain, rounding each stage's output to bf16 as the
-    GPU stores it; the pivot indices are compared bit for bit at both steps."""
+    The oracle runs the same chain on its own results, each stage's output
+    stored as bf16 as the GPU stores it; the pivot indices are compared bit for
+    bit at both steps and every output row of each stage against the oracle's."""
     w = WORKLOADS["pruned_1024px"]
     inp = make_inputs(w)
     B, H, D = w.batch, w.heads, w.head_dim
@@ -258,13 +270,13 @@ def test_pruned_chain_1024px():
     o10 = torch.empty_like(q10, device=DEV)
     V.var_attn_dense(p, 10, q10.to(DEV), k, v, o10)
     torch.cuda.synchronize()
-    rows10 = sample_rows(B, H, 1600, 48, seed=10)
-    assert_close(o10.reshape(-1, D)[torch.as_tensor(rows10, device=DEV)],
-                 oracle.attention(q10, inp.k, inp.v, cache_len(w.sides, 10), rows=rows10), "chain step 10")
-    prev = o10
+    ref10 = oracle.attention(q10, inp.k, inp.v, cache_len(w.sides, 10))
+    assert_close(o10, ref10, "chain step 10")
+    prev, prev_ref = o10, to_bf16(ref10)
     for step, num, den in ((11, 2, 5), (12, 1, 5)):
         x = inp.x[step]
         N = x.shape[1]
+        L = cache_len(w.sides, step)
         K = V.var_keep_count(N, num, den)
         idx_g, _ = gpu_pivot(p, step, x, K)
         idx_ref, _ = oracle.pivot_select(x, K)
@@ -275,14 +287,10 @@ def test_pruned_chain_1024px():
         out = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=DEV)
         V.var_restore_scatter(p, step, prev, oc, idx_d, K, out)
         torch.cuda.synchronize()
-        # oracle restore on the GPU's own bf16 inputs of this stage
-        ref = oracle.restore_scatter(prev.cpu(), oc.cpu(), idx_g, w.sides[step])
-        assert_close(out, ref, f"chain restore step {step}")
-        # sampled pruned rows against the oracle
-        crow = sample_rows(B, H, K, 32, seed=step)
-        bh, j = crow // K, crow % K
-        qrows = bh * N + idx_g[bh // H, j]
-        ref_rows = oracle.attention(inp.q[step], inp.k, inp.v, cache_len(w.sides, step), rows=qrows)
-        assert_close(oc.reshape(-1, D)[torch.as_tensor(crow, device=DEV)], ref_rows, f"chain pruned {step}")
-        prev = out
+        qrows = (np.arange(B * H)[:, None] * N + idx_ref[np.arange(B * H) // H]).reshape(-1)
+        oc_ref = oracle.attention(inp.q[step], inp.k, inp.v, L, rows=qrows)
+        assert_close(oc.reshape(-1, D), oc_ref, f"chain pruned rows {step}")
+        ref = oracle.restore_scatter(prev_ref, to_bf16(oc_ref).reshape(B, H, K, D), idx_ref, w.sides[step])
+        assert_close(out, ref, f"chain restore step {step}, every row")
+        prev, prev_ref = out, to_bf16(ref)
     check_device_status()

@@ -22,6 +22,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libvarattn.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "varattn.h")
+TEST_HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "varattn_test.h")
 MAX_SCALES = 32
 
 VAR_OK = 0
@@ -42,7 +43,7 @@ class VarError(RuntimeError):
 class var_problem(C.Structure):
     _fields_ = [("batch", C.c_int32), ("heads", C.c_int32), ("head_dim", C.c_int32),
                 ("n_scales", C.c_int32), ("side", C.c_int32 * MAX_SCALES),
-                ("kv_capacity", C.c_int32), ("softmax_scale", C.c_float)]
+                ("kv_capacity", C.c_int32), ("softmax_scale", C.c_float), ("status", C.c_void_p)]
 
 
 class var_block_mask(C.Structure):
@@ -86,7 +87,10 @@ _SIGS = {
     "var_sparvar_scores": (C.c_int, [_PROB, C.c_int32, C.c_int32, _P, _P, _P, C.c_size_t, _P, _P]),
     "var_sparvar_mask_build": (C.c_int, [_PROB, C.c_int32, C.c_int32, C.c_int32, _P, C.c_double, _P, _P,
                                          C.c_int32, _P, _P, _P]),
-    "var_selftest_wait_timeout": (C.c_int, [C.c_int32, _P]),
+    "var_selftest_wait_timeout": (C.c_int, [C.c_int32, _P, _P]),
+    "var_check_status": (C.c_int, [_P, _P, C.c_int32, _P]),
+    "var_test_mock_cuda": (C.c_int, [C.c_int32, C.c_int64]),
+    "var_test_mock_calls": (C.c_int64, []),
     "var_workspace_bytes": (C.c_size_t, [_PROB, C.c_int32, C.c_int32, C.c_int32]),
     "var_keep_count": (C.c_int32, [C.c_int32, C.c_int32, C.c_int32]),
     "var_status_string": (C.c_char_p, [C.c_int]),
@@ -99,9 +103,13 @@ for _name, (_res, _args) in _SIGS.items():
 
 
 def header_functions() -> Sequence[str]:
-    """Names of the functions include/varattn.h declares."""
-    text = open(HEADER_PATH).read()
-    return re.findall(r"^\s*VAR_API\s+(?:int|int32_t|size_t|const char\*)\s+(var_\w+)\s*\(", text, re.M)
+    """Names of the functions include/varattn.h and include/varattn_test.h declare."""
+    names = []
+    for path in (HEADER_PATH, TEST_HEADER_PATH):
+        text = open(path).read()
+        names += re.findall(r"^\s*VAR_API\s+(?:int|int32_t|int64_t|size_t|const char\*)\s+(var_\w+)\s*\(",
+                            text, re.M)
+    return names
 
 
 def lib() -> C.CDLL:
@@ -109,7 +117,9 @@ def lib() -> C.CDLL:
 
 
 def problem(batch: int, heads: int, head_dim: int, sides: Sequence[int], kv_capacity: int = 0,
-            softmax_scale: float = 0.0) -> var_problem:
+            softmax_scale: float = 0.0, status: Optional[torch.Tensor] = None) -> var_problem:
+    """The problem statement; `status`: an optional int32 device tensor whose first
+    element is the calls' own status word (var_problem.status)."""
     p = var_problem()
     p.batch, p.heads, p.head_dim = batch, heads, head_dim
     p.n_scales = len(sides)
@@ -117,6 +127,7 @@ def problem(batch: int, heads: int, head_dim: int, sides: Sequence[int], kv_capa
         p.side[i] = s
     p.kv_capacity = kv_capacity
     p.softmax_scale = softmax_scale
+    p.status = None if status is None else status.data_ptr()
     return p
 
 
@@ -148,6 +159,15 @@ def var_keep_count(n: int, num: int, den: int) -> int:
 def var_device_status(clear: bool = True) -> int:
     out = C.c_int32(0)
     _check("var_device_status", _lib.var_device_status(C.byref(out), 1 if clear else 0))
+    return out.value
+
+
+def var_check_status(status: Optional[torch.Tensor], clear: bool = True, stream=None) -> int:
+    """Read (and clear) a caller-owned status word (int32 device tensor; None = the
+    per-device word) in the order of `stream`."""
+    out = C.c_int32(0)
+    _check("var_check_status", _lib.var_check_status(_ptr(status), C.byref(out), 1 if clear else 0,
+                                                     _stream(stream)))
     return out.value
 
 
@@ -236,9 +256,10 @@ def var_workspace_bytes(p: var_problem, step: int, channels: int, keep_k: int) -
     return _lib.var_workspace_bytes(C.byref(p), step, channels, keep_k)
 
 
-def var_selftest_wait_timeout(limit_us: int, stream=None) -> None:
-    """Diagnostics: a kernel whose bounded wait gives up and records VAR_ERR_TIMEOUT."""
-    _check("var_selftest_wait_timeout", _lib.var_selftest_wait_timeout(limit_us, _stream(stream)))
+def var_selftest_wait_timeout(limit_us: int, status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Diagnostics: a kernel whose bounded wait gives up and records VAR_ERR_TIMEOUT
+    in `status` (None = the per-device word)."""
+    _check("var_selftest_wait_timeout", _lib.var_selftest_wait_timeout(limit_us, _ptr(status), _stream(stream)))
 
 
 def var_sparvar_units(p: var_problem, decision_step: int, sink_max_side: int) -> Tuple[int, int]:

@@ -10,7 +10,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libvarattn.so")
-SOURCES = ["api.cu", "attn.cu", "blocksparse.cu", "pivot.cu", "restore.cu", "saliency.cu", "sparvar.cu", "selftest.cu"]
+SOURCES = ["rt.cu", "api.cu", "attn.cu", "blocksparse.cu", "pivot.cu", "restore.cu", "saliency.cu", "sparvar.cu", "selftest.cu"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
@@ -20,6 +20,7 @@ FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hid
 def _deps_mtime() -> float:
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
     files.append(os.path.join(os.path.dirname(HERE), "include", "varattn.h"))
+    files.append(os.path.join(os.path.dirname(HERE), "include", "varattn_test.h"))
     files.append(os.path.abspath(__file__))
     return max(os.path.getmtime(f) for f in files)
 

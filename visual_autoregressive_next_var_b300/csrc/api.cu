@@ -10,8 +10,9 @@
 
 namespace varattn {
 
-// One status word per device that loads this library.  Kernels record the first
-// fault they detect (CAS from 0); var_device_status() reads and clears it.
+// One status word per device that loads this library, for calls whose problem
+// names no status word of its own.  Kernels record the first fault they detect
+// (CAS from 0); var_device_status() reads and clears it.
 static __device__ int32_t g_status_word;
 
 static std::mutex g_mu;
@@ -20,12 +21,42 @@ int32_t* device_status_ptr()
 {
     static int32_t* cache[64] = {};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (current_device(&dev) != cudaSuccess) return nullptr;
+    if (rt_mocked()) {
+        void* p = nullptr;
+        return rt().get_symbol_address(&p, reinterpret_cast<const void*>(&g_status_word)) == cudaSuccess
+                   ? static_cast<int32_t*>(p)
+                   : nullptr;
+    }
     std::lock_guard<std::mutex> lk(g_mu);
     if (!cache[dev]) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        if (rt().get_symbol_address(&p, reinterpret_cast<const void*>(&g_status_word)) != cudaSuccess || !p)
+            return nullptr;
         cache[dev] = static_cast<int32_t*>(p);
+    }
+    return cache[dev];
+}
+
+int32_t* status_word(const var_problem* p)
+{
+    if (p && p->status) return p->status;
+    return device_status_ptr();
+}
+
+int sm_count()
+{
+    static std::mutex mu;
+    static int cache[64] = {};
+    int dev = 0;
+    if (current_device(&dev) != cudaSuccess) return 0;
+    int n = 0;
+    if (rt_mocked())
+        return rt().device_attribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0 ? n : 0;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!cache[dev]) {
+        if (rt().device_attribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 0;
+        cache[dev] = n;
     }
     return cache[dev];
 }
@@ -33,19 +64,6 @@ int32_t* device_status_ptr()
 int encode_tmap_bf16(CUtensorMap* out, const void* base, int rank, const uint64_t* dims,
                      const uint64_t* strides_bytes, const uint32_t* box)
 {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        if (!fn) {
-            void* p = nullptr;
-            cudaDriverEntryPointQueryResult q;
-            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                                 &q) != cudaSuccess ||
-                q != cudaDriverEntryPointSuccess || !p)
-                return VAR_ERR_CUDA;
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-        }
-    }
     cuuint64_t d[5];
     cuuint64_t s[4];
     cuuint32_t b[5];
@@ -56,17 +74,16 @@ int encode_tmap_bf16(CUtensorMap* out, const void* base, int rank, const uint64_
         e[i] = 1;
         if (i + 1 < rank) s[i] = strides_bytes[i];
     }
-    const CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
-                          const_cast<void*>(base), d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUresult r = rt().encode_tiled(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+                                         const_cast<void*>(base), d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? VAR_OK : VAR_ERR_CUDA;
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Validate the problem and resolve the geometry of `step`.
-static int resolve(const var_problem* p, int32_t step, StepGeom* g)
+int resolve(const var_problem* p, int32_t step, StepGeom* g)
 {
     if (!p) return VAR_ERR_INVALID_ARG;
     if (p->batch <= 0 || p->heads <= 0 || p->n_scales <= 0 || p->n_scales > VAR_MAX_SCALES)
@@ -83,6 +100,7 @@ static int resolve(const var_problem* p, int32_t step, StepGeom* g)
     if (cap < L) return VAR_ERR_INVALID_ARG;
     if (static_cast<long long>(p->batch) * p->heads > 65535ll * 64) return VAR_ERR_UNSUPPORTED;
     if (!(p->softmax_scale >= 0.f) || !std::isfinite(p->softmax_scale)) return VAR_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(p->status) & 3u) return VAR_ERR_INVALID_ARG;
     g->B = p->batch;
     g->H = p->heads;
     g->D = p->head_dim;
@@ -92,6 +110,18 @@ static int resolve(const var_problem* p, int32_t step, StepGeom* g)
     g->cap = static_cast<int>(cap);
     g->scale = p->softmax_scale == 0.f ? 1.0f / std::sqrt(static_cast<float>(p->head_dim))
                                        : p->softmax_scale;
+    return VAR_OK;
+}
+
+int check_pivot_args(const var_problem* p, int32_t step, const void* x, int32_t channels, int32_t keep_k,
+                     const int32_t* idx, StepGeom* g)
+{
+    if (int rc = resolve(p, step, g)) return rc;
+    if (!x || channels <= 0 || channels % 32 != 0 || channels > 16384) return VAR_ERR_INVALID_ARG;
+    if (keep_k < 0 || keep_k > g->N) return VAR_ERR_INVALID_ARG;
+    if (keep_k > 0 && !idx) return VAR_ERR_INVALID_ARG;
+    if (g->N > 16384) return VAR_ERR_UNSUPPORTED;
+    if (!aligned16(x)) return VAR_ERR_UNSUPPORTED;
     return VAR_OK;
 }
 
@@ -108,7 +138,9 @@ int var_attn_dense(const var_problem* p, int32_t step, const void* q, const void
     if (int rc = resolve(p, step, &g)) return rc;
     if (!q || !k || !v || !o) return VAR_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return VAR_ERR_UNSUPPORTED;
-    return launch_attn_dense(g, q, k, v, o, static_cast<cudaStream_t>(stream));
+    int32_t* status = status_word(p);
+    if (!status) return VAR_ERR_CUDA;
+    return launch_attn_dense(g, q, k, v, o, static_cast<cudaStream_t>(stream), status);
 }
 
 size_t var_pivot_workspace_bytes(const var_problem* p, int32_t step, int32_t channels)
@@ -123,17 +155,14 @@ int var_pivot_select(const var_problem* p, int32_t step, const void* x, int32_t 
                      size_t workspace_bytes, void* stream)
 {
     StepGeom g;
-    if (int rc = resolve(p, step, &g)) return rc;
-    if (!x || channels <= 0 || channels % 32 != 0 || channels > 16384) return VAR_ERR_INVALID_ARG;
-    if (keep_k < 0 || keep_k > g.N) return VAR_ERR_INVALID_ARG;
-    if (keep_k > 0 && !idx) return VAR_ERR_INVALID_ARG;
-    if (g.N > 16384) return VAR_ERR_UNSUPPORTED;
-    if (!aligned16(x)) return VAR_ERR_UNSUPPORTED;
+    if (int rc = check_pivot_args(p, step, x, channels, keep_k, idx, &g)) return rc;
     const size_t need = pivot_workspace_bytes(g.B, g.N, channels);
     if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return VAR_ERR_WORKSPACE;
+    int32_t* status = status_word(p);
+    if (!status) return VAR_ERR_CUDA;
     return launch_pivot_select(g.B, g.N, channels, x, keep_k, idx, scores, workspace,
-                               workspace_bytes, static_cast<cudaStream_t>(stream));
+                               workspace_bytes, static_cast<cudaStream_t>(stream), status);
 }
 
 int var_attn_pruned(const var_problem* p, int32_t step, const void* q, const void* k, const void* v,
@@ -146,7 +175,10 @@ int var_attn_pruned(const var_problem* p, int32_t step, const void* q, const voi
     if (!q || !k || !v || !idx || !o_compact) return VAR_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_compact))
         return VAR_ERR_UNSUPPORTED;
-    return launch_attn_pruned(g, q, k, v, idx, keep_k, o_compact, static_cast<cudaStream_t>(stream), false);
+    int32_t* status = status_word(p);
+    if (!status) return VAR_ERR_CUDA;
+    return launch_attn_pruned(g, q, k, v, idx, keep_k, o_compact, static_cast<cudaStream_t>(stream), status,
+                              false);
 }
 
 int var_attn_pruned_scatter(const var_problem* p, int32_t step, const void* q, const void* k, const void* v,
@@ -158,7 +190,9 @@ int var_attn_pruned_scatter(const var_problem* p, int32_t step, const void* q, c
     if (keep_k == 0) return VAR_OK;
     if (!q || !k || !v || !idx || !out) return VAR_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return VAR_ERR_UNSUPPORTED;
-    return launch_attn_pruned(g, q, k, v, idx, keep_k, out, static_cast<cudaStream_t>(stream), true);
+    int32_t* status = status_word(p);
+    if (!status) return VAR_ERR_CUDA;
+    return launch_attn_pruned(g, q, k, v, idx, keep_k, out, static_cast<cudaStream_t>(stream), status, true);
 }
 
 int var_restore_fill(const var_problem* p, int32_t step, const void* prev, const int32_t* idx, int32_t keep_k,
@@ -170,8 +204,10 @@ int var_restore_fill(const var_problem* p, int32_t step, const void* prev, const
     if (keep_k < 0 || keep_k > g.N) return VAR_ERR_INVALID_ARG;
     if (!prev || !out || (keep_k > 0 && !idx)) return VAR_ERR_INVALID_ARG;
     if (!aligned16(prev) || !aligned16(out)) return VAR_ERR_UNSUPPORTED;
+    int32_t* status = status_word(p);
+    if (!status) return VAR_ERR_CUDA;
     return launch_restore_scatter(g.B, g.H, g.D, p->side[step - 1], g.side, prev, nullptr, idx, keep_k, out,
-                                  static_cast<cudaStream_t>(stream), true);
+                                  static_cast<cudaStream_t>(stream), status, true);
 }
 
 int var_attn_dense_lse(const var_problem* p, int32_t step, const void* q, const void* k, const void* v, void* o,
@@ -181,7 +217,9 @@ int var_attn_dense_lse(const var_problem* p, int32_t step, const void* q, const 
     if (int rc = resolve(p, step, &g)) return rc;
     if (!q || !k || !v || !o || !lse) return VAR_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return VAR_ERR_UNSUPPORTED;
-    return launch_attn_dense(g, q, k, v, o, static_cast<cudaStream_t>(stream), lse);
+    int32_t* status = status_word(p);
+    if (!status) return VAR_ERR_CUDA;
+    return launch_attn_dense(g, q, k, v, o, static_cast<cudaStream_t>(stream), status, lse);
 }
 
 int var_attn_saliency(const var_problem* p, int32_t src_step, const void* q_src, const void* k, const float* lse,
@@ -191,7 +229,9 @@ int var_attn_saliency(const var_problem* p, int32_t src_step, const void* q_src,
     if (int rc = resolve(p, src_step, &g)) return rc;
     if (!q_src || !k || !lse || !sal) return VAR_ERR_INVALID_ARG;
     if (!aligned16(q_src) || !aligned16(k)) return VAR_ERR_UNSUPPORTED;
-    return launch_saliency(g, g.N, g.L, q_src, k, lse, sal, static_cast<cudaStream_t>(stream));
+    int32_t* status = status_word(p);
+    if (!status) return VAR_ERR_CUDA;
+    return launch_saliency(g, g.N, g.L, q_src, k, lse, sal, static_cast<cudaStream_t>(stream), status);
 }
 
 size_t var_guided_pivot_workspace_bytes(const var_problem* p, int32_t step)
@@ -213,8 +253,10 @@ int var_guided_pivot_select(const var_problem* p, int32_t step, int32_t src_step
     if (!workspace || workspace_bytes < guided_workspace_bytes(g.B, g.N) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return VAR_ERR_WORKSPACE;
+    int32_t* status = status_word(p);
+    if (!status) return VAR_ERR_CUDA;
     return launch_guided_pivot(g.B, g.H, p->side[src_step], g.side, sal, keep_k, idx, scores, workspace,
-                               workspace_bytes, static_cast<cudaStream_t>(stream));
+                               workspace_bytes, static_cast<cudaStream_t>(stream), status);
 }
 
 int var_attn_dense_halved(const var_problem* p, int32_t step, const void* q, const void* k, const void* v,
@@ -225,7 +267,9 @@ int var_attn_dense_halved(const var_problem* p, int32_t step, const void* q, con
     if (g.B % 2 != 0) return VAR_ERR_INVALID_ARG;
     if (!q || !k || !v || !o) return VAR_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return VAR_ERR_UNSUPPORTED;
-    return launch_attn_dense_halved(g, q, k, v, o, static_cast<cudaStream_t>(stream));
+    int32_t* status = status_word(p);
+    if (!status) return VAR_ERR_CUDA;
+    return launch_attn_dense_halved(g, q, k, v, o, static_cast<cudaStream_t>(stream), status);
 }
 
 int var_restore_scatter(const var_problem* p, int32_t step, const void* prev, const void* o_compact,
@@ -238,8 +282,10 @@ int var_restore_scatter(const var_problem* p, int32_t step, const void* prev, co
     if (!prev || !out || (keep_k > 0 && (!o_compact || !idx))) return VAR_ERR_INVALID_ARG;
     if (!aligned16(prev) || !aligned16(out) || (keep_k > 0 && !aligned16(o_compact)))
         return VAR_ERR_UNSUPPORTED;
+    int32_t* status = status_word(p);
+    if (!status) return VAR_ERR_CUDA;
     return launch_restore_scatter(g.B, g.H, g.D, p->side[step - 1], g.side, prev, o_compact, idx,
-                                  keep_k, out, static_cast<cudaStream_t>(stream), false);
+                                  keep_k, out, static_cast<cudaStream_t>(stream), status, false);
 }
 
 int var_block_mask_build(const var_problem* p, int32_t step, int32_t qblock_side, int32_t radius,
@@ -435,10 +481,13 @@ size_t var_workspace_bytes(const var_problem* p, int32_t step, int32_t channels,
     return var_pivot_workspace_bytes(p, step, channels);
 }
 
-int var_selftest_wait_timeout(int32_t limit_us, void* stream)
+int var_selftest_wait_timeout(int32_t limit_us, int32_t* status, void* stream)
 {
     if (limit_us <= 0 || limit_us > 10000000) return VAR_ERR_INVALID_ARG;
-    return varattn::launch_wait_timeout(limit_us, static_cast<cudaStream_t>(stream));
+    if (reinterpret_cast<uintptr_t>(status) & 3u) return VAR_ERR_INVALID_ARG;
+    int32_t* word = status ? status : varattn::device_status_ptr();
+    if (!word) return VAR_ERR_CUDA;
+    return varattn::launch_wait_timeout(limit_us, static_cast<cudaStream_t>(stream), word);
 }
 
 int var_sparvar_units(const var_problem* p, int32_t decision_step, int32_t sink_max_side, int32_t* n_units_out,
@@ -468,8 +517,10 @@ int var_sparvar_scores(const var_problem* p, int32_t decision_step, int32_t sink
     if (!q || !k || !workspace || !scores) return VAR_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(scores) & 7))
         return VAR_ERR_UNSUPPORTED;
+    int32_t* status = status_word(p);
+    if (!status) return VAR_ERR_CUDA;
     return varattn::launch_sparvar_scores(g, m, q, k, workspace, workspace_bytes, scores,
-                                          static_cast<cudaStream_t>(stream));
+                                          static_cast<cudaStream_t>(stream), status);
 }
 
 int var_sparvar_mask_build(const var_problem* p, int32_t decision_step, int32_t step, int32_t sink_max_side,
@@ -563,8 +614,10 @@ int var_attn_blocksparse(const var_problem* p, int32_t step, const void* q, cons
     const int nb = g.side / mask->qblock_side;
     if (mask->n_qblocks != nb * nb || mask->sink_len < 0 || mask->sink_len > g.L || mask->nnz < 0)
         return VAR_ERR_INVALID_ARG;
+    int32_t* status = status_word(p);
+    if (!status) return VAR_ERR_CUDA;
     return launch_attn_blocksparse(g, p->side, p->n_scales, step, q, k, v, mask, o,
-                                   static_cast<cudaStream_t>(stream));
+                                   static_cast<cudaStream_t>(stream), status);
 }
 
 int32_t var_keep_count(int32_t n, int32_t num, int32_t den)
@@ -589,15 +642,36 @@ const char* var_status_string(int status)
 
 int var_device_status(int32_t* status_out, int32_t clear)
 {
+    if (!status_out) return VAR_ERR_INVALID_ARG;
     int32_t* p = device_status_ptr();
-    if (!p || !status_out) return VAR_ERR_CUDA;
-    if (cudaDeviceSynchronize() != cudaSuccess) return VAR_ERR_CUDA;
+    if (!p) return VAR_ERR_CUDA;
+    if (rt().device_sync() != cudaSuccess) return VAR_ERR_CUDA;
     int32_t v = 0;
-    if (cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return VAR_ERR_CUDA;
+    if (rt().memcpy_async(&v, p, sizeof v, cudaMemcpyDeviceToHost, nullptr) != cudaSuccess ||
+        rt().stream_sync(nullptr) != cudaSuccess)
+        return VAR_ERR_CUDA;
     *status_out = v;
     if (clear && v != 0) {
-        const int32_t z = 0;
-        if (cudaMemcpy(p, &z, sizeof z, cudaMemcpyHostToDevice) != cudaSuccess) return VAR_ERR_CUDA;
+        if (rt().memset_async(p, 0, sizeof v, nullptr) != cudaSuccess || rt().stream_sync(nullptr) != cudaSuccess)
+            return VAR_ERR_CUDA;
+    }
+    return VAR_OK;
+}
+
+int var_check_status(const int32_t* status, int32_t* status_out, int32_t clear, void* stream)
+{
+    if (!status_out || (reinterpret_cast<uintptr_t>(status) & 3u)) return VAR_ERR_INVALID_ARG;
+    int32_t* p = status ? const_cast<int32_t*>(status) : device_status_ptr();
+    if (!p) return VAR_ERR_CUDA;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    if (rt().memcpy_async(&v, p, sizeof v, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        rt().stream_sync(st) != cudaSuccess)
+        return VAR_ERR_CUDA;
+    *status_out = v;
+    if (clear && v != 0) {
+        if (rt().memset_async(p, 0, sizeof v, st) != cudaSuccess || rt().stream_sync(st) != cudaSuccess)
+            return VAR_ERR_CUDA;
     }
     return VAR_OK;
 }

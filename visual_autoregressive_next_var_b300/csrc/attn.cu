@@ -37,28 +37,12 @@ static double dispatch_makespan(int pairs, int singles, int n_sms)
     return end;
 }
 
-static int sm_count()
+static TilePlan plan_tiles(int bh, int tiles_per_bh, int n_sms)
 {
-    static std::mutex mu;
-    static int cache[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    std::lock_guard<std::mutex> lk(mu);
-    if (!cache[dev]) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-        cache[dev] = n;
-    }
-    return cache[dev];
-}
-
-static TilePlan plan_tiles(int bh, int tiles_per_bh)
-{
-    const int n_sms = sm_count();
     static std::mutex mu;
     static std::map<std::tuple<int, int, int>, TilePlan> cache;
     const auto key = std::make_tuple(bh, tiles_per_bh, n_sms);
-    {
+    if (!rt_mocked()) {
         std::lock_guard<std::mutex> lk(mu);
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
@@ -73,6 +57,7 @@ static TilePlan plan_tiles(int bh, int tiles_per_bh)
         dispatch_makespan(b.n_pair_ctas, b.grid - b.n_pair_ctas, n_sms) <
             dispatch_makespan(a.n_pair_ctas, a.grid - a.n_pair_ctas, n_sms) - 1e-9)
         best = b;
+    if (rt_mocked()) return best;
     std::lock_guard<std::mutex> lk(mu);
     cache[key] = best;
     return best;
@@ -82,21 +67,13 @@ static TilePlan plan_tiles(int bh, int tiles_per_bh)
 
 template <int D, int MODE>
 static int launch_attn(const StepGeom& g, const void* q, const void* k, const void* v,
-                       const int32_t* idx, int n_rows, void* o, cudaStream_t st, bool halved = false,
-                       bool scatter = false, float* lse = nullptr, int v_cap = 0)
+                       const int32_t* idx, int n_rows, void* o, cudaStream_t st, int32_t* status,
+                       bool halved = false, bool scatter = false, float* lse = nullptr, int v_cap = 0)
 {
     using Lay = AttnLayout<D>;
-    static bool attr_done = false;   // per process; the attribute is per function
     auto kern = attn_kernel<D, MODE, DenseMaps>;
-    if (!attr_done) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::SMEM_BYTES) !=
-            cudaSuccess)
-            return VAR_ERR_CUDA;
-        attr_done = true;
-    }
-    int32_t* status = device_status_ptr();
-    if (!status) return VAR_ERR_CUDA;
     if (n_rows == 0) return VAR_OK;
+    if (ensure_smem_attr(kern, Lay::SMEM_BYTES) != cudaSuccess) return VAR_ERR_CUDA;
 
     DenseMaps maps;
     CUtensorMap& tq = maps.q;
@@ -126,7 +103,9 @@ static int launch_attn(const StepGeom& g, const void* q, const void* k, const vo
     a.heads = g.H;
     a.tiles_per_bh = (n_rows + 127) / 128;
     a.slots_per_bh = a.tiles_per_bh / 2;
-    const TilePlan plan = plan_tiles(static_cast<int>(BH_run), a.tiles_per_bh);
+    const int n_sms = sm_count();
+    if (n_sms <= 0) return VAR_ERR_CUDA;
+    const TilePlan plan = plan_tiles(static_cast<int>(BH_run), a.tiles_per_bh, n_sms);
     a.n_pair_ctas = plan.n_pair_ctas;
     a.n_conv_slots = plan.n_conv_slots;
     a.n_kv = (g.L + 127) / 128;
@@ -138,41 +117,42 @@ static int launch_attn(const StepGeom& g, const void* q, const void* k, const vo
     a.scatter = scatter ? 1 : 0;
     a.lse = lse;
     a.status = status;
-    const dim3 grid(static_cast<unsigned>(plan.grid));
-    kern<<<grid, 384, Lay::SMEM_BYTES, st>>>(maps, a);
-    return cuda_status(cudaGetLastError());
+    return cuda_status(launch_kernel(kern, dim3(static_cast<unsigned>(plan.grid)), dim3(384), Lay::SMEM_BYTES, st,
+                                     false, maps, a));
 }
 
 int launch_attn_dense(const StepGeom& g, const void* q, const void* k, const void* v, void* o,
-                      cudaStream_t st, float* lse)
+                      cudaStream_t st, int32_t* status, float* lse)
 {
-    if (g.D == 128) return launch_attn<128, MODE_DENSE>(g, q, k, v, nullptr, g.N, o, st, false, false, lse);
-    if (g.D == 64) return launch_attn<64, MODE_DENSE>(g, q, k, v, nullptr, g.N, o, st, false, false, lse);
+    if (g.D == 128) return launch_attn<128, MODE_DENSE>(g, q, k, v, nullptr, g.N, o, st, status, false, false, lse);
+    if (g.D == 64) return launch_attn<64, MODE_DENSE>(g, q, k, v, nullptr, g.N, o, st, status, false, false, lse);
     return VAR_ERR_UNSUPPORTED;
 }
 
 int launch_attn_dense_vcap(const StepGeom& g, const void* q, const void* k, const void* v, int v_cap, void* o,
-                           cudaStream_t st)
+                           cudaStream_t st, int32_t* status)
 {
     if (v_cap < g.L) return VAR_ERR_INVALID_ARG;
-    if (g.D == 128) return launch_attn<128, MODE_DENSE>(g, q, k, v, nullptr, g.N, o, st, false, false, nullptr, v_cap);
-    if (g.D == 64) return launch_attn<64, MODE_DENSE>(g, q, k, v, nullptr, g.N, o, st, false, false, nullptr, v_cap);
+    if (g.D == 128)
+        return launch_attn<128, MODE_DENSE>(g, q, k, v, nullptr, g.N, o, st, status, false, false, nullptr, v_cap);
+    if (g.D == 64)
+        return launch_attn<64, MODE_DENSE>(g, q, k, v, nullptr, g.N, o, st, status, false, false, nullptr, v_cap);
     return VAR_ERR_UNSUPPORTED;
 }
 
 int launch_attn_pruned(const StepGeom& g, const void* q, const void* k, const void* v,
-                       const int32_t* idx, int keep_k, void* o, cudaStream_t st, bool scatter)
+                       const int32_t* idx, int keep_k, void* o, cudaStream_t st, int32_t* status, bool scatter)
 {
-    if (g.D == 128) return launch_attn<128, MODE_GATHER>(g, q, k, v, idx, keep_k, o, st, false, scatter);
-    if (g.D == 64) return launch_attn<64, MODE_GATHER>(g, q, k, v, idx, keep_k, o, st, false, scatter);
+    if (g.D == 128) return launch_attn<128, MODE_GATHER>(g, q, k, v, idx, keep_k, o, st, status, false, scatter);
+    if (g.D == 64) return launch_attn<64, MODE_GATHER>(g, q, k, v, idx, keep_k, o, st, status, false, scatter);
     return VAR_ERR_UNSUPPORTED;
 }
 
 int launch_attn_dense_halved(const StepGeom& g, const void* q, const void* k, const void* v, void* o,
-                             cudaStream_t st)
+                             cudaStream_t st, int32_t* status)
 {
-    if (g.D == 128) return launch_attn<128, MODE_DENSE>(g, q, k, v, nullptr, g.N, o, st, true);
-    if (g.D == 64) return launch_attn<64, MODE_DENSE>(g, q, k, v, nullptr, g.N, o, st, true);
+    if (g.D == 128) return launch_attn<128, MODE_DENSE>(g, q, k, v, nullptr, g.N, o, st, status, true);
+    if (g.D == 64) return launch_attn<64, MODE_DENSE>(g, q, k, v, nullptr, g.N, o, st, status, true);
     return VAR_ERR_UNSUPPORTED;
 }
 

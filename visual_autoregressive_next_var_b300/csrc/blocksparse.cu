@@ -16,19 +16,10 @@ namespace varattn {
 
 template <int D>
 static int launch_sparse(const StepGeom& g, const int32_t* sides, int step, const void* q, const void* k,
-                         const void* v, const var_block_mask* mask, void* o, cudaStream_t st)
+                         const void* v, const var_block_mask* mask, void* o, cudaStream_t st, int32_t* status)
 {
     using Lay = AttnLayout<D>;
-    static bool attr_done = false;
     auto kern = attn_kernel<D, MODE_SPARSE, SparseMaps>;
-    if (!attr_done) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::SMEM_BYTES_SPARSE) !=
-            cudaSuccess)
-            return VAR_ERR_CUDA;
-        attr_done = true;
-    }
-    int32_t* status = device_status_ptr();
-    if (!status) return VAR_ERR_CUDA;
 
     // The sink range must end exactly at a scale boundary of the leading scales.
     int first_local = 0;
@@ -38,6 +29,7 @@ static int launch_sparse(const StepGeom& g, const int32_t* sides, int step, cons
         ++first_local;
     }
     if (cum != mask->sink_len) return VAR_ERR_INVALID_ARG;
+    if (ensure_smem_attr(kern, Lay::SMEM_BYTES_SPARSE) != cudaSuccess) return VAR_ERR_CUDA;
 
     SparseMaps maps;
     std::memset(&maps, 0, sizeof maps);
@@ -104,18 +96,19 @@ static int launch_sparse(const StepGeom& g, const int32_t* sides, int step, cons
     }
     const uint64_t ctas = BH * static_cast<uint64_t>(a.nsq) * a.nsq;
     if (ctas > 0x7fffffffull) return VAR_ERR_UNSUPPORTED;
-    kern<<<static_cast<unsigned>(ctas), 384, Lay::SMEM_BYTES_SPARSE, st>>>(maps, a);
-    return cuda_status(cudaGetLastError());
+    return cuda_status(launch_kernel(kern, dim3(static_cast<unsigned>(ctas)), dim3(384), Lay::SMEM_BYTES_SPARSE, st,
+                                     false, maps, a));
 }
 
 int launch_attn_blocksparse(const StepGeom& g, const int32_t* sides, int n_scales, int step, const void* q,
-                            const void* k, const void* v, const var_block_mask* mask, void* o, cudaStream_t st)
+                            const void* k, const void* v, const var_block_mask* mask, void* o, cudaStream_t st,
+                            int32_t* status)
 {
     (void)n_scales;
     if (mask->qblock_side != 8) return VAR_ERR_UNSUPPORTED;
     if (g.side % 8 != 0) return VAR_ERR_UNSUPPORTED;
-    if (g.D == 128) return launch_sparse<128>(g, sides, step, q, k, v, mask, o, st);
-    if (g.D == 64) return launch_sparse<64>(g, sides, step, q, k, v, mask, o, st);
+    if (g.D == 128) return launch_sparse<128>(g, sides, step, q, k, v, mask, o, st, status);
+    if (g.D == 64) return launch_sparse<64>(g, sides, step, q, k, v, mask, o, st, status);
     return VAR_ERR_UNSUPPORTED;
 }
 

@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/varattn.h"
+#include "rt.h"
 
 namespace varattn {
 
@@ -29,36 +30,49 @@ struct StepGeom {
     float scale;     // softmax scale
 };
 
+// Validate the problem and resolve the geometry of `step` (host only, no CUDA call).
+int resolve(const var_problem* p, int32_t step, StepGeom* g);
+
 // Device address of this library's status word on the current device (0 on error).
 int32_t* device_status_ptr();
+
+// The status word the kernels of a call with problem p record faults in: the
+// caller's p->status, else the per-device word (0 on error).
+int32_t* status_word(const var_problem* p);
+
+// The argument checks of pivot selection, shared by the workspace and the
+// allocation-free entry points (geometry in *g).
+int check_pivot_args(const var_problem* p, int32_t step, const void* x, int32_t channels, int32_t keep_k,
+                     const int32_t* idx, StepGeom* g);
 
 // 3-D / 4-D bf16 tensor maps with 128-byte swizzle, box inner extent 64 elements.
 // dims/strides as cuTensorMapEncodeTiled takes them (strides in bytes, rank-1 of them).
 int encode_tmap_bf16(CUtensorMap* out, const void* base, int rank, const uint64_t* dims,
                      const uint64_t* strides_bytes, const uint32_t* box);
 
+// Launchers: `status` is the device status word of the call.
 int launch_attn_dense(const StepGeom& g, const void* q, const void* k, const void* v, void* o,
-                      cudaStream_t st, float* lse = nullptr);
+                      cudaStream_t st, int32_t* status, float* lse = nullptr);
 // As launch_attn_dense with V read at its own stride of v_cap rows per (b,h).
 int launch_attn_dense_vcap(const StepGeom& g, const void* q, const void* k, const void* v, int v_cap, void* o,
-                           cudaStream_t st);
+                           cudaStream_t st, int32_t* status);
 int launch_attn_pruned(const StepGeom& g, const void* q, const void* k, const void* v,
-                       const int32_t* idx, int keep_k, void* o, cudaStream_t st, bool scatter);
+                       const int32_t* idx, int keep_k, void* o, cudaStream_t st, int32_t* status, bool scatter);
 int launch_attn_dense_halved(const StepGeom& g, const void* q, const void* k, const void* v, void* o,
-                             cudaStream_t st);
+                             cudaStream_t st, int32_t* status);
 int launch_attn_blocksparse(const StepGeom& g, const int32_t* sides, int n_scales, int step,
                             const void* q, const void* k, const void* v,
-                            const var_block_mask* mask, void* o, cudaStream_t st);
+                            const var_block_mask* mask, void* o, cudaStream_t st, int32_t* status);
 size_t pivot_workspace_bytes(int B, int N, int C);
 int launch_pivot_select(int B, int N, int C, const void* x, int keep_k, int32_t* idx,
-                        float* scores, void* ws, size_t ws_bytes, cudaStream_t st);
+                        float* scores, void* ws, size_t ws_bytes, cudaStream_t st, int32_t* status);
 int launch_select_exact(int B, int N, int keep_k, const float* keys_lo, const float* keys_hi, int* band_idx,
-                        double* band_score, int32_t* idx, cudaStream_t st);
+                        double* band_score, int32_t* idx, cudaStream_t st, int32_t* status);
 int launch_saliency(const StepGeom& g, int n_src, int L_src, const void* q, const void* k, const float* lse,
-                    float* sal, cudaStream_t st);
+                    float* sal, cudaStream_t st, int32_t* status);
 size_t guided_workspace_bytes(int B, int N);
 int launch_guided_pivot(int B, int H, int sp, int s, const float* sal, int keep_k, int32_t* idx, float* scores,
-                        void* ws, size_t ws_bytes, cudaStream_t st);
+                        void* ws, size_t ws_bytes, cudaStream_t st, int32_t* status);
 // The decision step's 64-key units (dynamic sparse pattern): the sink range
 // [0, sink_len) in 64-token chunks (units [0, n_sink)), then every 8x8 key block
 // of each later scale up to the decision scale, row-major, scale by scale.
@@ -71,12 +85,16 @@ struct UnitMap {
 };
 size_t sparvar_workspace_bytes(const StepGeom& g);
 // One-thread kernel whose wait gives up after limit_us and records VAR_ERR_TIMEOUT.
-int launch_wait_timeout(int limit_us, cudaStream_t st);
+int launch_wait_timeout(int limit_us, cudaStream_t st, int32_t* status);
 int launch_sparvar_scores(const StepGeom& g, const UnitMap& m, const void* q, const void* k, void* ws,
-                          size_t ws_bytes, double* scores, cudaStream_t st);
+                          size_t ws_bytes, double* scores, cudaStream_t st, int32_t* status);
 int launch_restore_scatter(int B, int H, int D, int sp, int s, const void* prev, const void* oc,
-                           const int32_t* idx, int keep_k, void* out, cudaStream_t st, bool fill_only);
+                           const int32_t* idx, int keep_k, void* out, cudaStream_t st, int32_t* status,
+                           bool fill_only);
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? VAR_OK : VAR_ERR_CUDA; }
+
+// SM count of the current device (0 if it cannot be read).
+int sm_count();
 
 }  // namespace varattn

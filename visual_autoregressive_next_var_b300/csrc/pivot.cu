@@ -879,28 +879,14 @@ __global__ void __launch_bounds__(kSelThreads, 1)
 size_t pivot_workspace_bytes(int B, int N, int C) { return pivot_ws_layout(B, N, C).total; }
 
 int launch_pivot_select(int B, int N, int C, const void* xv, int keep_k, int32_t* idx, float* scores,
-                        void* ws, size_t ws_bytes, cudaStream_t st)
+                        void* ws, size_t ws_bytes, cudaStream_t st, int32_t* status)
 {
     const PivotWs w = pivot_ws_layout(B, N, C);
     if (ws_bytes < w.total) return VAR_ERR_WORKSPACE;
     if (N > kMaxN || C > 16384) return VAR_ERR_UNSUPPORTED;
-    int32_t* status = device_status_ptr();
-    if (!status) return VAR_ERR_CUDA;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return VAR_ERR_CUDA;
-    {
-        static std::mutex mu;
-        static bool attr[64] = {};
-        std::lock_guard<std::mutex> lk(mu);
-        if (!attr[dev]) {
-            if (cudaFuncSetAttribute(pivot_colsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kRingBytes) != cudaSuccess ||
-                cudaFuncSetAttribute(pivot_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     16384 * 4) != cudaSuccess)
-                return VAR_ERR_CUDA;
-            attr[dev] = true;
-        }
-    }
+    if (ensure_smem_attr(pivot_colsum_kernel, kRingBytes) != cudaSuccess ||
+        ensure_smem_attr(pivot_score_kernel, 16384 * 4) != cudaSuccess)
+        return VAR_ERR_CUDA;
     auto* base = static_cast<uint8_t*>(ws);
     auto* m64 = reinterpret_cast<double*>(base + w.mean64);
     auto* m32 = reinterpret_cast<float*>(base + w.mean32);
@@ -910,57 +896,35 @@ int launch_pivot_select(int B, int N, int C, const void* xv, int keep_k, int32_t
     auto* bsc = reinterpret_cast<double*>(base + w.band_score);
     const auto* x = static_cast<const __nv_bfloat16*>(xv);
 
-    {
-        const dim3 grid(kSlabs, (C + kChunk - 1) / kChunk, B);
-        pivot_colsum_kernel<<<grid, kSumThreads, kRingBytes, st>>>(x, N, C, m64, m32, status);
-        if (cudaGetLastError() != cudaSuccess) return VAR_ERR_CUDA;
-    }
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at[0].val.programmaticStreamSerializationAllowed = 1;
-    {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((N + kScoreTok - 1) / kScoreTok, B, 1);
-        cfg.blockDim = dim3(kScoreThreads, 1, 1);
-        cfg.dynamicSmemBytes = static_cast<size_t>(C) * 4;
-        cfg.stream = st;
-        cfg.attrs = at;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, pivot_score_kernel, x, N, C, static_cast<const float*>(m32), lok, hik, scores,
-                               status) != cudaSuccess)
-            return VAR_ERR_CUDA;
-    }
+    if (launch_kernel(pivot_colsum_kernel, dim3(kSlabs, (C + kChunk - 1) / kChunk, B), dim3(kSumThreads), kRingBytes,
+                      st, false, x, N, C, m64, m32, status) != cudaSuccess)
+        return VAR_ERR_CUDA;
+    // the score and select kernels start as programmatic dependents of their predecessor
+    if (launch_kernel(pivot_score_kernel, dim3((N + kScoreTok - 1) / kScoreTok, B, 1), dim3(kScoreThreads),
+                      static_cast<size_t>(C) * 4, st, true, x, N, C, m32, lok, hik, scores, status) != cudaSuccess)
+        return VAR_ERR_CUDA;
     if (keep_k > 0) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(B, 1, 1);
-        cfg.blockDim = dim3(kSelThreads, 1, 1);
-        cfg.dynamicSmemBytes = 0;
-        cfg.stream = st;
-        cfg.attrs = at;
-        cfg.numAttrs = 1;
         auto* fn = N <= 4 * kSelThreads ? pivot_select_kernel<4>
                    : N <= 8 * kSelThreads ? pivot_select_kernel<8>
                                           : pivot_select_kernel<kMaxKeysPerThread>;
-        if (cudaLaunchKernelEx(&cfg, fn, x, N, C, keep_k, static_cast<const float*>(lok),
-                               static_cast<const float*>(hik), static_cast<const double*>(m64), bidx, bsc, idx,
-                               status, 0) != cudaSuccess)
+        if (launch_kernel(fn, dim3(B), dim3(kSelThreads), 0, st, true, x, N, C, keep_k, lok, hik, m64, bidx, bsc, idx,
+                          status, 0) != cudaSuccess)
             return VAR_ERR_CUDA;
     }
     return VAR_OK;
 }
 
 int launch_select_exact(int B, int N, int keep_k, const float* keys_lo, const float* keys_hi, int* band_idx,
-                        double* band_score, int32_t* idx, cudaStream_t st)
+                        double* band_score, int32_t* idx, cudaStream_t st, int32_t* status)
 {
     if (N > kMaxN) return VAR_ERR_UNSUPPORTED;
-    int32_t* status = device_status_ptr();
-    if (!status) return VAR_ERR_CUDA;
     auto* fn = N <= 4 * kSelThreads ? pivot_select_kernel<4>
                : N <= 8 * kSelThreads ? pivot_select_kernel<8>
                                       : pivot_select_kernel<kMaxKeysPerThread>;
-    fn<<<B, kSelThreads, 0, st>>>(nullptr, N, 32, keep_k, keys_lo, keys_hi, nullptr, band_idx, band_score, idx,
-                                  status, 1);
-    return cuda_status(cudaGetLastError());
+    const __nv_bfloat16* no_x = nullptr;
+    const double* no_mean = nullptr;
+    return cuda_status(launch_kernel(fn, dim3(B), dim3(kSelThreads), 0, st, false, no_x, N, 32, keep_k, keys_lo,
+                                     keys_hi, no_mean, band_idx, band_score, idx, status, 1));
 }
 
 // ---------------------------------------------------------------------------
@@ -987,11 +951,16 @@ static uint8_t* pivot_scratch_ptr()
     static std::mutex mu;
     static uint8_t* cache[64] = {};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (current_device(&dev) != cudaSuccess) return nullptr;
+    void* p = nullptr;
+    if (rt_mocked())
+        return rt().get_symbol_address(&p, reinterpret_cast<const void*>(g_pivot_scratch)) == cudaSuccess
+                   ? static_cast<uint8_t*>(p)
+                   : nullptr;
     std::lock_guard<std::mutex> lk(mu);
     if (!cache[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_pivot_scratch) != cudaSuccess || !p) return nullptr;
+        if (rt().get_symbol_address(&p, reinterpret_cast<const void*>(g_pivot_scratch)) != cudaSuccess || !p)
+            return nullptr;
         cache[dev] = static_cast<uint8_t*>(p);
     }
     return cache[dev];
@@ -1004,21 +973,16 @@ extern "C" int var_pivot_select_noalloc(const var_problem* p, int32_t step, cons
                                         void* stream)
 {
     using namespace varattn;
-    if (!p || step < 0 || step >= p->n_scales || p->n_scales > VAR_MAX_SCALES) return VAR_ERR_INVALID_ARG;
-    if (p->batch <= 0 || p->side[step] <= 0 || p->side[step] > 4096) return VAR_ERR_INVALID_ARG;
-    if (!x || channels <= 0 || channels % 32 != 0) return VAR_ERR_INVALID_ARG;
-    const int B = p->batch;
-    const int N = p->side[step] * p->side[step];
-    if (keep_k < 0 || keep_k > N) return VAR_ERR_INVALID_ARG;
-    if (keep_k > 0 && !idx) return VAR_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(x) & 15u) != 0) return VAR_ERR_UNSUPPORTED;
-    if (B > kNoAllocMaxB || N > kNoAllocMaxN || channels > kNoAllocMaxC) return VAR_ERR_WORKSPACE;
-    const size_t need = pivot_workspace_bytes(B, N, channels);
-    if (need > kNoAllocBytes) return VAR_ERR_WORKSPACE;
+    StepGeom g;
+    if (int rc = check_pivot_args(p, step, x, channels, keep_k, idx, &g)) return rc;
+    if (g.B > kNoAllocMaxB || g.N > kNoAllocMaxN || channels > kNoAllocMaxC) return VAR_ERR_WORKSPACE;
+    if (pivot_workspace_bytes(g.B, g.N, channels) > kNoAllocBytes) return VAR_ERR_WORKSPACE;
+    int32_t* status = status_word(p);
+    if (!status) return VAR_ERR_CUDA;
     uint8_t* ws = pivot_scratch_ptr();
     if (!ws) return VAR_ERR_CUDA;
     // Nothing in the scratch needs clearing: every word is written before it
     // is read within a call.
-    return launch_pivot_select(B, N, channels, x, keep_k, idx, scores, ws, kNoAllocBytes,
-                               static_cast<cudaStream_t>(stream));
+    return launch_pivot_select(g.B, g.N, channels, x, keep_k, idx, scores, ws, kNoAllocBytes,
+                               static_cast<cudaStream_t>(stream), status);
 }

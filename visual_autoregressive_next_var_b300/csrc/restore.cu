@@ -99,8 +99,10 @@ __global__ void __launch_bounds__(256)
 }
 
 int launch_restore_scatter(int B, int H, int D, int sp, int s, const void* prev, const void* oc,
-                           const int32_t* idx, int keep_k, void* out, cudaStream_t st, bool fill_only)
+                           const int32_t* idx, int keep_k, void* out, cudaStream_t st, int32_t* status,
+                           bool fill_only)
 {
+    (void)status;
     const int N = s * s;
     const dim3 grid((N + kRestoreTok - 1) / kRestoreTok, B * H);
     if (B * H > 65535) return VAR_ERR_UNSUPPORTED;
@@ -108,13 +110,14 @@ int launch_restore_scatter(int B, int H, int D, int sp, int s, const void* prev,
     auto* P = static_cast<const __nv_bfloat16*>(prev);
     auto* C = static_cast<const __nv_bfloat16*>(oc);
     auto* O = static_cast<__nv_bfloat16*>(out);
+    const int fill = fill_only ? 1 : 0;
     if (D == 128)
-        restore_scatter_kernel<128><<<grid, 256, 0, st>>>(P, C, idx, keep_k, O, H, sp, s, ratio, fill_only);
-    else if (D == 64)
-        restore_scatter_kernel<64><<<grid, 256, 0, st>>>(P, C, idx, keep_k, O, H, sp, s, ratio, fill_only);
-    else
-        return VAR_ERR_UNSUPPORTED;
-    return cuda_status(cudaGetLastError());
+        return cuda_status(launch_kernel(restore_scatter_kernel<128>, grid, dim3(256), 0, st, false, P, C, idx, keep_k,
+                                         O, H, sp, s, ratio, fill));
+    if (D == 64)
+        return cuda_status(launch_kernel(restore_scatter_kernel<64>, grid, dim3(256), 0, st, false, P, C, idx, keep_k,
+                                         O, H, sp, s, ratio, fill));
+    return VAR_ERR_UNSUPPORTED;
 }
 
 }  // namespace varattn

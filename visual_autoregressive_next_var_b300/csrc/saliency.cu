@@ -285,24 +285,10 @@ inline GuidedWs guided_ws_layout(int B, int N)
 
 template <int D>
 int launch_saliency_d(const StepGeom& g, int n_src, int L_src, const void* q, const void* k, const float* lse,
-                      float* sal, cudaStream_t st)
+                      float* sal, cudaStream_t st, int32_t* status)
 {
     using Lay = SalLayout<D>;
-    {
-        static std::mutex mu;
-        static bool done[64] = {};
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return VAR_ERR_CUDA;
-        std::lock_guard<std::mutex> lk(mu);
-        if (!done[dev]) {
-            if (cudaFuncSetAttribute(saliency_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     Lay::SMEM_BYTES) != cudaSuccess)
-                return VAR_ERR_CUDA;
-            done[dev] = true;
-        }
-    }
-    int32_t* status = device_status_ptr();
-    if (!status) return VAR_ERR_CUDA;
+    if (ensure_smem_attr(saliency_kernel<D>, Lay::SMEM_BYTES) != cudaSuccess) return VAR_ERR_CUDA;
     SalMaps maps;
     const uint64_t BH = static_cast<uint64_t>(g.B) * g.H;
     const uint32_t box[3] = {64, 128, 1};
@@ -327,24 +313,24 @@ int launch_saliency_d(const StepGeom& g, int n_src, int L_src, const void* q, co
     a.status = status;
     const uint64_t grid = BH * static_cast<uint64_t>(a.key_tiles);
     if (grid > 0x7fffffffull) return VAR_ERR_UNSUPPORTED;
-    saliency_kernel<D><<<static_cast<unsigned>(grid), 256, Lay::SMEM_BYTES, st>>>(maps, a);
-    return cuda_status(cudaGetLastError());
+    return cuda_status(launch_kernel(saliency_kernel<D>, dim3(static_cast<unsigned>(grid)), dim3(256), Lay::SMEM_BYTES,
+                                     st, false, maps, a));
 }
 
 }  // namespace
 
 int launch_saliency(const StepGeom& g, int n_src, int L_src, const void* q, const void* k, const float* lse,
-                    float* sal, cudaStream_t st)
+                    float* sal, cudaStream_t st, int32_t* status)
 {
-    if (g.D == 128) return launch_saliency_d<128>(g, n_src, L_src, q, k, lse, sal, st);
-    if (g.D == 64) return launch_saliency_d<64>(g, n_src, L_src, q, k, lse, sal, st);
+    if (g.D == 128) return launch_saliency_d<128>(g, n_src, L_src, q, k, lse, sal, st, status);
+    if (g.D == 64) return launch_saliency_d<64>(g, n_src, L_src, q, k, lse, sal, st, status);
     return VAR_ERR_UNSUPPORTED;
 }
 
 size_t guided_workspace_bytes(int B, int N) { return guided_ws_layout(B, N).total; }
 
 int launch_guided_pivot(int B, int H, int sp, int s, const float* sal, int keep_k, int32_t* idx, float* scores,
-                        void* ws, size_t ws_bytes, cudaStream_t st)
+                        void* ws, size_t ws_bytes, cudaStream_t st, int32_t* status)
 {
     const int N = s * s;
     const GuidedWs w = guided_ws_layout(B, N);
@@ -353,13 +339,13 @@ int launch_guided_pivot(int B, int H, int sp, int s, const float* sal, int keep_
     auto* lo = reinterpret_cast<float*>(base + w.lo);
     auto* hi = reinterpret_cast<float*>(base + w.hi);
     const dim3 grid((N + 255) / 256, B);
-    guided_upsample_kernel<<<grid, 256, 0, st>>>(sal, H, sp, s, static_cast<float>(sp) / static_cast<float>(s),
-                                                 1.0f / (static_cast<float>(H) * static_cast<float>(sp * sp)), lo, hi,
-                                                 scores);
-    if (cudaGetLastError() != cudaSuccess) return VAR_ERR_CUDA;
+    if (launch_kernel(guided_upsample_kernel, grid, dim3(256), 0, st, false, sal, H, sp, s,
+                      static_cast<float>(sp) / static_cast<float>(s),
+                      1.0f / (static_cast<float>(H) * static_cast<float>(sp * sp)), lo, hi, scores) != cudaSuccess)
+        return VAR_ERR_CUDA;
     if (keep_k == 0) return VAR_OK;
     return launch_select_exact(B, N, keep_k, lo, hi, reinterpret_cast<int*>(base + w.band_idx),
-                               reinterpret_cast<double*>(base + w.band_score), idx, st);
+                               reinterpret_cast<double*>(base + w.band_score), idx, st, status);
 }
 
 }  // namespace varattn

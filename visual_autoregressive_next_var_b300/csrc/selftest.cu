@@ -1,6 +1,6 @@
 // Diagnostics: a bounded wait that is made to give up.  One thread waits on
 // an mbarrier that nothing arrives on; the wait returns after its time limit
-// and the kernel records VAR_ERR_TIMEOUT in the device status word, as a
+// and the kernel records VAR_ERR_TIMEOUT in the call's status word, as a
 // pipeline wait of the attention kernels would, then exits.  No fault, no
 // hang: the device stays usable.
 #include "internal.h"
@@ -22,12 +22,10 @@ __global__ void wait_timeout_kernel(uint64_t limit_ns, int32_t* status)
 
 }  // namespace
 
-int launch_wait_timeout(int limit_us, cudaStream_t st)
+int launch_wait_timeout(int limit_us, cudaStream_t st, int32_t* status)
 {
-    int32_t* status = device_status_ptr();
-    if (!status) return VAR_ERR_CUDA;
-    wait_timeout_kernel<<<1, 32, 0, st>>>(static_cast<uint64_t>(limit_us) * 1000ull, status);
-    return cudaGetLastError() == cudaSuccess ? VAR_OK : VAR_ERR_CUDA;
+    return cuda_status(launch_kernel(wait_timeout_kernel, dim3(1), dim3(32), 0, st, false,
+                                     static_cast<uint64_t>(limit_us) * 1000ull, status));
 }
 
 }  // namespace varattn

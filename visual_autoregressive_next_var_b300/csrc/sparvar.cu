@@ -91,7 +91,7 @@ size_t sparvar_workspace_bytes(const StepGeom& g)
 }
 
 int launch_sparvar_scores(const StepGeom& g, const UnitMap& m, const void* q, const void* k, void* ws,
-                          size_t ws_bytes, double* scores, cudaStream_t st)
+                          size_t ws_bytes, double* scores, cudaStream_t st, int32_t* status)
 {
     if (ws_bytes < sparvar_workspace_bytes(g)) return VAR_ERR_WORKSPACE;
     const int BH = g.B * g.H;
@@ -101,14 +101,19 @@ int launch_sparvar_scores(const StepGeom& g, const UnitMap& m, const void* q, co
     for (int u0 = 0; u0 < m.U; u0 += g.D) {
         const long long n = static_cast<long long>(BH) * g.L * (g.D / 8);
         const unsigned blocks = static_cast<unsigned>(std::min<long long>((n + 255) / 256, 148ll * 16));
-        if (g.D == 128) unit_indicator_kernel<128><<<blocks, 256, 0, st>>>(m, BH, u0, v_ind);
-        else unit_indicator_kernel<64><<<blocks, 256, 0, st>>>(m, BH, u0, v_ind);
-        if (cudaGetLastError() != cudaSuccess) return VAR_ERR_CUDA;
-        if (int rc = launch_attn_dense_vcap(g, q, k, v_ind, g.L, o, st)) return rc;
+        const cudaError_t e1 = g.D == 128
+                                   ? launch_kernel(unit_indicator_kernel<128>, dim3(blocks), dim3(256), 0, st, false,
+                                                   m, BH, u0, v_ind)
+                                   : launch_kernel(unit_indicator_kernel<64>, dim3(blocks), dim3(256), 0, st, false,
+                                                   m, BH, u0, v_ind);
+        if (e1 != cudaSuccess) return VAR_ERR_CUDA;
+        if (int rc = launch_attn_dense_vcap(g, q, k, v_ind, g.L, o, st, status)) return rc;
         const unsigned nqb = static_cast<unsigned>((g.side / 8) * (g.side / 8));
-        if (g.D == 128) unit_score_kernel<128><<<nqb, 8 * 128, 0, st>>>(o, BH, g.side, m.U, u0, scores);
-        else unit_score_kernel<64><<<nqb, 8 * 64, 0, st>>>(o, BH, g.side, m.U, u0, scores);
-        if (cudaGetLastError() != cudaSuccess) return VAR_ERR_CUDA;
+        const cudaError_t e2 = g.D == 128 ? launch_kernel(unit_score_kernel<128>, dim3(nqb), dim3(8 * 128), 0, st,
+                                                          false, o, BH, g.side, m.U, u0, scores)
+                                          : launch_kernel(unit_score_kernel<64>, dim3(nqb), dim3(8 * 64), 0, st, false,
+                                                          o, BH, g.side, m.U, u0, scores);
+        if (e2 != cudaSuccess) return VAR_ERR_CUDA;
     }
     return VAR_OK;
 }
