@@ -103,7 +103,7 @@ def load_peaks():
     if os.path.exists(path):
         d = json.load(open(path))
         return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
-                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained") or d["bf16_tflops"], "source": "measured"}
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
             "source": "fallback"}
 
@@ -654,7 +654,8 @@ def run_gpu(args):
         r = {"ms": t, "kernel": KERNEL_NAMES[name]}
         if name in step.flops:
             r["TFLOP/s"] = step.flops[name] / t / 1e9
-            r["frac_tensor"] = r["TFLOP/s"] / peaks["bf16_tflops"]
+            r["frac_tensor"] = r["TFLOP/s"] / peaks["bf16_tflops_sustained"]       # timed inside the long step
+            r["frac_tensor_of_burst"] = r["TFLOP/s"] / peaks["bf16_tflops"]
             r["effective_dense_equiv_TFLOP/s"] = step.flops_dense_equiv[name] / t / 1e9
         else:
             r["GB/s"] = step.bytes[name] / t / 1e6
@@ -666,9 +667,14 @@ def run_gpu(args):
     dom_name = ROW_NAMES[dom]
     if dom_name in step.flops:
         achieved = step.flops[dom_name] / per_row[dom] / 1e9
+        # the kernel is timed inside a step of ~3 ms of back-to-back tensor work,
+        # so its peak is the sustained cuBLAS figure (the burst one is beside it)
         roof = {"kernel": KERNEL_NAMES[dom_name], "row": dom_name, "bound": "tensor", "achieved": achieved,
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                "peak_source": f"{peaks['source']} dense bf16 burst (cuBLAS)",
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops_sustained"],
+                "peak_source": f"{peaks['source']} dense bf16 sustained (cuBLAS, seconds-long loop under the "
+                               "power cap)",
+                "frac_of_burst": achieved / peaks["bf16_tflops"],
                 "traffic": ncu_traffic(TRAFFIC_KEYS[dom_name]) if dom_name in TRAFFIC_KEYS else None,
                 "algorithmic_flops_per_launch": step.flops[dom_name], "launch_ms": per_row[dom]}
     else:
