@@ -247,7 +247,8 @@ def sparvar_units(sides: Sequence[int], d: int, sink_max_side: int):
 def sparvar_scores(q_d: torch.Tensor, k: torch.Tensor, sides: Sequence[int], d: int, sink_max_side: int,
                    scale: Optional[float] = None) -> np.ndarray:
     """A[qb, u] fp64: unit u's attention mass averaged over the 64 queries of the
-    decision step's 8x8 query block qb (row-major blocks), heads and batch."""
+    decision step's 8x8 query block qb (row-major blocks), heads and batch: the
+    sum over (b, h, y, x) in that order, divided by B * H * 64."""
     B, H, N, D = q_d.shape
     s_d = sides[d]
     assert N == s_d * s_d and s_d % 8 == 0
@@ -261,7 +262,16 @@ def sparvar_scores(q_d: torch.Tensor, k: torch.Tensor, sides: Sequence[int], d: 
         raise ValueError("oracle_unit_mass failed")
     nb = s_d // 8
     g = mass.reshape(B, H, nb, 8, nb, 8, U)            # [b, h, by, y, bx, x, u]
-    return g.sum(axis=(0, 1, 3, 5)).reshape(nb * nb, U) / (B * H * 64)
+    # The per-query masses of a block are added one at a time in the order
+    # (b, h, y, x), starting from 0, in fp64: a fixed order, so the rounding
+    # of the sum is defined (the pages fix none).
+    acc = np.zeros((nb, nb, U), dtype=np.float64)
+    for b in range(B):
+        for h in range(H):
+            for y in range(8):
+                for x in range(8):
+                    acc += g[b, h, :, y, :, x, :]
+    return acc.reshape(nb * nb, U) / (B * H * 64)
 
 
 def sparvar_select(A: np.ndarray, n_sink: int, tau: float):

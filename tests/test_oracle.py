@@ -409,6 +409,33 @@ def test_sparvar_unit_mass_matches_bruteforce():
     assert np.allclose(A.sum(axis=1), 1.0, rtol=0, atol=1e-12)   # every query's mass is 1
 
 
+def test_sparvar_block_score_sums_in_the_stated_order():
+    """The block score adds the 2 x 2 x 64 per-query masses one at a time in the
+    order (b, h, y, x), in fp64, then divides by B H 64: equal bit for bit to
+    that sequence of additions done with Python floats."""
+    B, H, D, d = 2, 2, 16, 4
+    L, N = cum(SV_SIDES, d), 16 * 16
+    q = randn_bf16((B, H, N, D), 711)
+    k = randn_bf16((B, H, L, D), 712)
+    unit_of, units, _ = oracle.sparvar_units(SV_SIDES, d, SV_SINK)
+    U = len(units)
+    mass = np.zeros((B, H, N, U))
+    lib = oracle.lib()
+    assert lib.oracle_unit_mass(B, H, N, L, L, D, 1.0 / np.sqrt(D), oracle._ptr(oracle._bits(q)),
+                                oracle._ptr(oracle._bits(k)), oracle._ptr(unit_of), U, oracle._ptr(mass)) == 0
+    A = oracle.sparvar_scores(q, k, SV_SIDES, d, SV_SINK)
+    for qb in range(4):
+        by, bx = divmod(qb, 2)
+        for u in range(U):
+            acc = 0.0
+            for b in range(B):
+                for h in range(H):
+                    for y in range(8):
+                        for x in range(8):
+                            acc += float(mass[b, h, (8 * by + y) * 16 + 8 * bx + x, u])
+            assert A[qb, u] == acc / (B * H * 64)
+
+
 def test_sparvar_unit_mass_uniform_closed_form():
     # q = 0: every key gets 1/L, so a unit's mass is its size over L
     B, H, D, d = 1, 2, 8, 4
