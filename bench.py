@@ -533,10 +533,16 @@ def extra_rows(V, dev, step: Step, inp, iters: int, peaks, host_bytes):
     # SparVAR dynamic pattern: the 32x32 step's block scores decide the 64x64 step's mask
     d_sv, tau_sv = src, 0.8
     U_sv, _ = V.var_sparvar_units(p, d_sv, SINK_SIDE)
-    sv_ws = torch.empty(V.var_sparvar_workspace_bytes(p, d_sv), dtype=torch.uint8, device=dev)
+    sv_ws = torch.empty(V.var_sparvar_workspace_bytes(p, d_sv, SINK_SIDE), dtype=torch.uint8, device=dev)
     nqb_sv = (int(round(Ns ** 0.5)) // 8) ** 2
     sv_sc = torch.empty((nqb_sv, U_sv), dtype=torch.float64, device=dev)
-    t_sc = time_graph(lambda: V.var_sparvar_scores(p, d_sv, SINK_SIDE, q_src, step.k, sv_ws, sv_sc), iters, flush)
+    sv_rs = torch.zeros(nqb_sv, dtype=torch.int32, device=dev)
+    t_sc = time_graph(lambda: V.var_sparvar_scores(p, d_sv, SINK_SIDE, tau_sv, q_src, step.k, sv_ws, sv_sc,
+                                                   rescored=sv_rs), iters, flush)
+    n_rescored = int(sv_rs.sum().item())
+    t_sc_all = time_graph(lambda: V.var_sparvar_scores(p, d_sv, SINK_SIDE, tau_sv, q_src, step.k, sv_ws, sv_sc,
+                                                       flags=V.VAR_SPARVAR_RESCORE_ALL), iters, flush)
+    V.var_sparvar_scores(p, d_sv, SINK_SIDE, tau_sv, q_src, step.k, sv_ws, sv_sc)
     t0 = time.perf_counter()
     A = sv_sc.cpu().numpy()
     rp, en, sink = V.var_sparvar_mask_build(p, d_sv, FINAL, SINK_SIDE, A, tau_sv)
@@ -550,10 +556,12 @@ def extra_rows(V, dev, step: Step, inp, iters: int, peaks, host_bytes):
     pairs = mask_kept_pairs(WORKLOADS[W1024].sides, rp, en, sink, QBLOCK)
     fl_sv = 4.0 * B * H * pairs * D
     rows["sparvar_dynamic_mask_32_to_64"] = {
-        "scores_ms": t_sc, "host_select_map_plan_ms": t_host, "attn_ms": t_sv,
+        "scores_ms": t_sc, "blocks_rescored_fp64": n_rescored, "blocks": nqb_sv,
+        "scores_all_blocks_fp64_ms": t_sc_all, "host_select_map_plan_ms": t_host, "attn_ms": t_sv,
         "density": pairs / (step.N[FINAL] * step.L[FINAL]), "TFLOP/s": fl_sv / t_sv / 1e9,
         "effective_dense_equiv_TFLOP/s": step.flops["attn_dense_1024px"] / t_sv / 1e9, "units": U_sv, "tau": tau_sv,
-        "note": "decision step 32x32: block scores -> host selection + index mapping -> block-sparse "
+        "note": "decision step 32x32: block scores (certified fp32 on the CUDA cores, fp64 re-score of the "
+                "blocks the bound does not settle) -> host selection + index mapping -> block-sparse "
                 "attention of the 64x64 step",
         "timing": "CUDA graph replay after an L2 flush; host part timed once"}
     del q_src, o_src, o_sv

@@ -379,23 +379,35 @@ VAR_API int var_attn_blocksparse(const var_problem* p, int32_t step, const void*
 VAR_API int var_sparvar_units(const var_problem* p, int32_t decision_step, int32_t sink_max_side,
                               int32_t* n_units_out, int32_t* n_sink_units_out);
 
-/* Device workspace bytes var_sparvar_scores needs (0 for an invalid problem). */
-VAR_API size_t var_sparvar_workspace_bytes(const var_problem* p, int32_t decision_step);
+/* Device workspace bytes var_sparvar_scores needs (0 for invalid arguments). */
+VAR_API size_t var_sparvar_workspace_bytes(const var_problem* p, int32_t decision_step, int32_t sink_max_side);
+
+/* var_sparvar_scores flag: re-score every block in fp64, not only the unsettled ones. */
+#define VAR_SPARVAR_RESCORE_ALL 1
 
 /*
  * Block scores of the decision step on the device: scores [n_qb][U] fp64
- * (n_qb = (side/8)^2, row-major query blocks; caller-owned device memory).
+ * (n_qb = (side/8)^2, row-major query blocks; caller-owned device memory),
+ * exact enough that the selection at this `tau` (var_sparvar_mask_build) keeps
+ * the units the fp64 definition keeps.  Each score is first computed in fp32
+ * with a rigorous error bound; a block whose selection the bounds do not settle
+ * is re-scored in fp64 in the definition's own evaluation order (softmax
+ * denominator and unit masses added key by key, the block sum over the batch,
+ * heads and the block's queries in that order).  Only two fp64 values closer
+ * than the last bits of a transcendental function's rounding can still be
+ * ordered differently from a CPU evaluation.
  * q: the decision step's queries [B][H][N][D]; k: the cache [B][H][kv_capacity][D].
- * The mass is computed as attention with the values replaced by each unit's
- * indicator (head_dim units per pass of the dense attention kernel), then
- * averaged in a fixed order.  workspace: var_sparvar_workspace_bytes bytes,
- * 16-byte aligned.  Asynchronous on `stream`.
- * Errors: as var_attn_dense, VAR_ERR_WORKSPACE (too small), and those of
- * var_sparvar_units.
+ * flags: 0 or VAR_SPARVAR_RESCORE_ALL.  rescored: optional device int32
+ * [n_qb], 1 where the block was re-scored in fp64.  workspace:
+ * var_sparvar_workspace_bytes bytes, 256-byte aligned.  At most 512 units.
+ * Asynchronous on `stream`.
+ * Errors: as var_attn_dense, VAR_ERR_INVALID_ARG (tau outside [0, 1], flags),
+ * VAR_ERR_WORKSPACE (too small), VAR_ERR_UNSUPPORTED (more than 512 units,
+ * alignment), and those of var_sparvar_units.
  */
-VAR_API int var_sparvar_scores(const var_problem* p, int32_t decision_step, int32_t sink_max_side,
-                               const void* q, const void* k, void* workspace, size_t workspace_bytes,
-                               double* scores, void* stream);
+VAR_API int var_sparvar_scores(const var_problem* p, int32_t decision_step, int32_t sink_max_side, double tau,
+                               int32_t flags, const void* q, const void* k, void* workspace,
+                               size_t workspace_bytes, double* scores, int32_t* rescored, void* stream);
 
 /*
  * HOST: the target step's block mask from the decision step's scores (host

@@ -38,3 +38,25 @@ def to_bf16(a: np.ndarray) -> torch.Tensor:
     """The oracle's own fp64 result stored as bf16 (round to nearest even through
     fp32), for chained stages whose next input is a stored bf16 tensor."""
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float64)).float().to(torch.bfloat16)
+
+
+def csr_to_token_mask(sides, step, qbs, row_ptr, entries, sink_len):
+    """Expand the library's block CSR into a [N, L] token mask (bool)."""
+    sq = sides[step]
+    nb = sq // qbs
+    offs = np.cumsum([0] + [s * s for s in sides[: step + 1]])
+    L = offs[-1]
+    out = np.zeros((sq * sq, L), dtype=bool)
+    for qb in range(nb * nb):
+        by, bx = divmod(qb, nb)
+        keys = np.zeros(L, dtype=bool)
+        keys[:sink_len] = True
+        for e in entries[row_ptr[qb]:row_ptr[qb + 1]]:
+            sc, u, w = e >> 24, (e >> 12) & 0xFFF, e & 0xFFF
+            s = sides[sc]
+            for r in range(u * qbs, min(s, u * qbs + qbs)):
+                c0, c1 = w * qbs, min(s, w * qbs + qbs)
+                keys[offs[sc] + r * s + c0: offs[sc] + r * s + c1] = True
+        for y in range(by * qbs, by * qbs + qbs):
+            out[y * sq + bx * qbs: y * sq + bx * qbs + qbs] = keys
+    return out

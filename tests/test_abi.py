@@ -10,6 +10,7 @@ import torch
 import oracle
 import visual_autoregressive_next_var_b300 as V
 from var_synth import SCHEDULE_1024, SCHEDULE_2K, SCHEDULE_256
+from tests._util import csr_to_token_mask as _csr_to_token_mask
 
 
 def test_library_exports_every_declared_symbol():
@@ -86,28 +87,6 @@ def test_pruned_restore_pivot_reject_bad_arguments():
     odd = V.problem(3, 16, 128, SCHEDULE_1024)
     assert L.var_attn_dense_halved(C.byref(odd), 12, f, f, f, f, None) == V.VAR_ERR_INVALID_ARG
     assert L.var_attn_dense_halved(C.byref(p), 12, f, None, f, f, None) == V.VAR_ERR_INVALID_ARG
-
-
-def _csr_to_token_mask(sides, step, qbs, row_ptr, entries, sink_len):
-    """Expand the library's block CSR into a [N, L] token mask."""
-    sq = sides[step]
-    nb = sq // qbs
-    offs = np.cumsum([0] + [s * s for s in sides[: step + 1]])
-    L = offs[-1]
-    out = np.zeros((sq * sq, L), dtype=bool)
-    for qb in range(nb * nb):
-        by, bx = divmod(qb, nb)
-        keys = np.zeros(L, dtype=bool)
-        keys[:sink_len] = True
-        for e in entries[row_ptr[qb]:row_ptr[qb + 1]]:
-            sc, u, w = e >> 24, (e >> 12) & 0xFFF, e & 0xFFF
-            s = sides[sc]
-            for r in range(u * qbs, min(s, u * qbs + qbs)):
-                c0, c1 = w * qbs, min(s, w * qbs + qbs)
-                keys[offs[sc] + r * s + c0: offs[sc] + r * s + c1] = True
-        for y in range(by * qbs, by * qbs + qbs):
-            out[y * sq + bx * qbs: y * sq + bx * qbs + qbs] = keys
-    return out
 
 
 @pytest.mark.parametrize("sides,qbs,radius,sink", [
@@ -242,8 +221,20 @@ def test_sparvar_rejects_bad_arguments():
     with pytest.raises(V.VarError):
         V.var_sparvar_mask_build(q, 5, 6, 4, np.full((9, 15), 1 / 15), 0.5)   # target side 36
     L = V.lib()
-    assert L.var_sparvar_workspace_bytes(None, 9) == 0
-    assert L.var_sparvar_scores(C.byref(p), 9, 16, None, None, None, 0, None, None) == V.VAR_ERR_INVALID_ARG
+    f = _fake()
+    assert L.var_sparvar_workspace_bytes(None, 9, 16) == 0
+    assert L.var_sparvar_workspace_bytes(C.byref(p), 7, 16) == 0              # side 20
+    ws = L.var_sparvar_workspace_bytes(C.byref(p), 9, 16)
+    assert ws > 0
+    sc = V.lib().var_sparvar_scores
+    assert sc(C.byref(p), 9, 16, 0.5, 0, None, None, None, 0, None, None, None) == V.VAR_ERR_INVALID_ARG
+    assert sc(C.byref(p), 9, 16, 1.5, 0, f, f, f, ws, f, None, None) == V.VAR_ERR_INVALID_ARG     # tau
+    assert sc(C.byref(p), 9, 16, -0.1, 0, f, f, f, ws, f, None, None) == V.VAR_ERR_INVALID_ARG
+    assert sc(C.byref(p), 9, 16, 0.5, 2, f, f, f, ws, f, None, None) == V.VAR_ERR_INVALID_ARG     # flags
+    assert sc(C.byref(p), 9, 16, 0.5, 0, f, f, f, ws - 1, f, None, None) == V.VAR_ERR_WORKSPACE
+    assert sc(C.byref(p), 9, 16, 0.5, 0, f, f, C.c_void_p(0x10010), ws, f, None, None) == V.VAR_ERR_UNSUPPORTED
+    big = V.problem(2, 16, 128, (1, 2, 4, 8, 16, 32, 64, 96, 128, 160))     # 6 + 16 + 64 + 144 + 256 + 400 units
+    assert sc(C.byref(big), 9, 16, 0.5, 0, f, f, f, 1 << 40, f, None, None) == V.VAR_ERR_UNSUPPORTED
 
 
 def test_selftest_wait_timeout_rejects_bad_limits():

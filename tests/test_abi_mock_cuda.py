@@ -33,7 +33,7 @@ def _cases(V):
     p64 = V.problem(1, 3, 64, sides)
     ws_piv = L.var_pivot_workspace_bytes(C.byref(p), 9, 256)
     ws_gd = L.var_guided_pivot_workspace_bytes(C.byref(p), 9)
-    ws_sv = L.var_sparvar_workspace_bytes(C.byref(p), 9)
+    ws_sv = L.var_sparvar_workspace_bytes(C.byref(p), 9, 16)
     m = V.var_block_mask()
     m.qblock_side, m.n_qblocks, m.sink_len, m.nnz = 8, 16, 521, 64
     m.row_ptr, m.entries = FAKE, FAKE
@@ -59,7 +59,7 @@ def _cases(V):
                                                                       None)),
         ("var_attn_blocksparse", lambda: L.var_attn_blocksparse(C.byref(p), 9, f, f, f, C.byref(m), f, None)),
         ("var_attn_blocksparse_plan", lambda: L.var_attn_blocksparse(C.byref(p), 9, f, f, f, C.byref(mp), f, None)),
-        ("var_sparvar_scores", lambda: L.var_sparvar_scores(C.byref(p), 9, 16, f, f, f, ws_sv, f, None)),
+        ("var_sparvar_scores", lambda: L.var_sparvar_scores(C.byref(p), 9, 16, 0.8, 0, f, f, f, ws_sv, f, fs, None)),
         ("var_selftest_wait_timeout", lambda: L.var_selftest_wait_timeout(1000, fs, None)),
         ("var_device_status", lambda: L.var_device_status(C.byref(out), 1)),
         ("var_check_status", lambda: L.var_check_status(fs, C.byref(out), 1, None)),

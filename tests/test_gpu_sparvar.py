@@ -1,7 +1,8 @@
-"""GPU parity: the SparVAR dynamic sparse pattern -- decision-step block scores
-(dense attention kernel on unit-indicator values + ordered reduction), the host
-selection and index mapping, and block-sparse attention under the resulting
-mask -- against the oracle."""
+"""GPU parity: the SparVAR dynamic sparse pattern -- the decision step's block
+scores (certified fp32, fp64 re-score of unsettled blocks), the host selection
+and index mapping, and block-sparse attention under the resulting mask --
+against the oracle's own pipeline: the mask the GPU path builds must equal,
+token for token, the mask the oracle builds from its own fp64 scores."""
 import numpy as np
 import pytest
 import torch
@@ -9,7 +10,7 @@ import torch
 import oracle
 import visual_autoregressive_next_var_b300 as V
 from var_synth import WORKLOADS, cache_len, make_inputs, randn_bf16
-from tests._util import assert_close, check_device_status
+from tests._util import assert_close, check_device_status, csr_to_token_mask
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -17,36 +18,58 @@ DEV = "cuda"
 SMALL = (1, 2, 4, 8, 16, 24, 32, 40, 48)      # sinks: the 1, 2, 4 scales at sink_max_side 4
 
 
-def gpu_scores(p, d, sink, q, k):
+def gpu_scores(p, d, sink, tau, q, k, flags=0):
     U, _ = V.var_sparvar_units(p, d, sink)
     nqb = (int(round(q.shape[2] ** 0.5)) // 8) ** 2
-    ws = torch.empty(V.var_sparvar_workspace_bytes(p, d), dtype=torch.uint8, device=DEV)
+    ws = torch.empty(V.var_sparvar_workspace_bytes(p, d, sink), dtype=torch.uint8, device=DEV)
     sc = torch.empty((nqb, U), dtype=torch.float64, device=DEV)
-    V.var_sparvar_scores(p, d, sink, q, k, ws, sc)
+    rs = torch.full((nqb,), -1, dtype=torch.int32, device=DEV)
+    V.var_sparvar_scores(p, d, sink, tau, q, k, ws, sc, rescored=rs, flags=flags)
     torch.cuda.synchronize()
-    return sc.cpu().numpy()
+    return sc.cpu().numpy(), rs.cpu().numpy()
 
 
-def check_scores(got, ref):
-    # each per-row unit mass is rounded to bf16 (relative 2^-9) before the average
-    assert np.all(np.abs(got - ref) <= 4e-3 * ref + 1e-7), np.max(np.abs(got - ref) / (ref + 1e-12))
-    assert np.allclose(got.sum(axis=1), 1.0, rtol=0, atol=4e-3)
+def gpu_mask(p, sides, d, ks, sink, A, tau):
+    rp, en, sink_len = V.var_sparvar_mask_build(p, d, ks, sink, A, tau)
+    return csr_to_token_mask(sides, ks, 8, rp, en, sink_len), (rp, en, sink_len)
 
 
-@pytest.mark.parametrize("d,D", [(5, 128), (5, 64), (8, 64)])   # (8, 64): 92 units, two passes
+def oracle_mask(sides, d, ks, sink, A_ref, tau):
+    _, units, ns = oracle.sparvar_units(sides, d, sink)
+    return oracle.sparvar_keep_mask(sides, d, ks, units, oracle.sparvar_select(A_ref, ns, tau), sink).astype(bool)
+
+
+def check_scores(got, rescored, ref):
+    """Certified blocks: within the fp32 path's accuracy; re-scored blocks: the
+    fp64 definition up to the last bits of exp."""
+    assert set(np.unique(rescored)) <= {0, 1}
+    for qb in range(got.shape[0]):
+        rel = np.abs(got[qb] - ref[qb]) / np.maximum(ref[qb], 1e-300)
+        if rescored[qb]:
+            assert np.max(rel) < 1e-13, (qb, np.max(rel))
+        else:
+            assert np.max(np.abs(got[qb] - ref[qb]) - 1e-4 * ref[qb]) <= 1e-12, (qb, np.max(rel))
+    assert np.allclose(got.sum(axis=1), 1.0, rtol=0, atol=1e-6)
+
+
+@pytest.mark.parametrize("d,D", [(5, 128), (5, 64), (8, 64)])   # (8, 64): 92 units
 def test_scores_match_oracle(d, D):
     B, H, sink = 2, 2, 4
     L, N = cache_len(SMALL, d), SMALL[d] ** 2
     q = randn_bf16((B, H, N, D), 1101 + d)
     k = randn_bf16((B, H, L + 64, D), 1102 + d)              # spare cache capacity
     p = V.problem(B, H, D, SMALL, kv_capacity=L + 64)
-    got = gpu_scores(p, d, sink, q.to(DEV), k.to(DEV))
-    check_scores(got, oracle.sparvar_scores(q, k, SMALL, d, sink))
+    ref = oracle.sparvar_scores(q, k, SMALL, d, sink)
+    got, rs = gpu_scores(p, d, sink, 0.7, q.to(DEV), k.to(DEV))
+    check_scores(got, rs, ref)
+    forced, rs2 = gpu_scores(p, d, sink, 0.7, q.to(DEV), k.to(DEV), flags=V.VAR_SPARVAR_RESCORE_ALL)
+    assert np.all(rs2 == 1)
+    check_scores(forced, rs2, ref)
     check_device_status()
 
 
 @pytest.mark.parametrize("tau", [0.5, 0.9])
-def test_dynamic_mask_attention_small(tau):
+def test_dynamic_mask_equals_oracle_and_attention_small(tau):
     B, H, D, sink, d, ks = 2, 2, 128, 4, 5, 7                 # 24 x 24 decides the 40 x 40 step
     L = cache_len(SMALL, ks)
     q_d = randn_bf16((B, H, SMALL[d] ** 2, D), 1111)
@@ -55,30 +78,40 @@ def test_dynamic_mask_attention_small(tau):
     v = randn_bf16((B, H, L, D), 1114)
     p = V.problem(B, H, D, SMALL, kv_capacity=L)             # the cache holds the target step's keys
     kd, vd = k.to(DEV), v.to(DEV)
-    A = gpu_scores(p, d, sink, q_d.to(DEV), kd)
-    rp, en, sink_len = V.var_sparvar_mask_build(p, d, ks, sink, A, tau)
+    A, _ = gpu_scores(p, d, sink, tau, q_d.to(DEV), kd)
+    got_mask, (rp, en, sink_len) = gpu_mask(p, SMALL, d, ks, sink, A, tau)
+    ref_mask = oracle_mask(SMALL, d, ks, sink, oracle.sparvar_scores(q_d, k, SMALL, d, sink), tau)
+    assert ref_mask.mean() < 1.0
+    assert np.array_equal(got_mask, ref_mask)
     plan = [torch.as_tensor(x, device=DEV) for x in V.var_block_mask_plan(p, ks, 8, rp, en, sink_len)]
     mask = V.block_mask_struct(8, torch.as_tensor(rp, device=DEV), torch.as_tensor(en, device=DEV), sink_len, plan)
     o = torch.empty_like(q, device=DEV)
     V.var_attn_blocksparse(p, ks, q.to(DEV), kd, vd, mask, o)
     torch.cuda.synchronize()
-    _, units, ns = oracle.sparvar_units(SMALL, d, sink)
-    keep = oracle.sparvar_keep_mask(SMALL, d, ks, units, oracle.sparvar_select(A, ns, tau), sink)
-    assert keep.mean() < 1.0
-    assert_close(o, oracle.attention_keep(q, k, v, L, keep), f"dynamic mask tau {tau}")
+    assert_close(o, oracle.attention_keep(q, k, v, L, ref_mask), f"dynamic mask tau {tau}")
     check_device_status()
 
 
 def test_dynamic_mask_1024px_decision_32_target_64():
     w = WORKLOADS["pruned_1024px"]
-    d, ks, sink, tau = 9, 12, 16, 0.8
+    d, ks, sink = 9, 12, 16
     inp = make_inputs(w, steps=(d, ks))
     B, H, D = w.batch, w.heads, w.head_dim
     p = V.problem(B, H, D, w.sides, kv_capacity=inp.k.shape[2])
     kd, vd = inp.k.to(DEV), inp.v.to(DEV)
-    A = gpu_scores(p, d, sink, inp.q[d].to(DEV), kd)
-    check_scores(A, oracle.sparvar_scores(inp.q[d], inp.k, w.sides, d, sink))
-    rp, en, sink_len = V.var_sparvar_mask_build(p, d, ks, sink, A, tau)
+    qd_d = inp.q[d].to(DEV)
+    A_ref = oracle.sparvar_scores(inp.q[d], inp.k, w.sides, d, sink)
+    for tau in (0.5, 0.8, 0.95):
+        A, rs = gpu_scores(p, d, sink, tau, qd_d, kd)
+        check_scores(A, rs, A_ref)
+        got_mask, (rp, en, sink_len) = gpu_mask(p, w.sides, d, ks, sink, A, tau)
+        ref_mask = oracle_mask(w.sides, d, ks, sink, A_ref, tau)
+        assert np.array_equal(got_mask, ref_mask), f"tau {tau}: {np.sum(got_mask != ref_mask)} tokens differ"
+    # attention of the 64x64 step under the tau = 0.8 mask, on sampled rows
+    tau = 0.8
+    A, _ = gpu_scores(p, d, sink, tau, qd_d, kd)
+    _, (rp, en, sink_len) = gpu_mask(p, w.sides, d, ks, sink, A, tau)
+    ref_mask = oracle_mask(w.sides, d, ks, sink, A_ref, tau)
     plan = [torch.as_tensor(x, device=DEV) for x in V.var_block_mask_plan(p, ks, 8, rp, en, sink_len)]
     mask = V.block_mask_struct(8, torch.as_tensor(rp, device=DEV), torch.as_tensor(en, device=DEV), sink_len, plan)
     q = inp.q[ks]
@@ -86,13 +119,30 @@ def test_dynamic_mask_1024px_decision_32_target_64():
     V.var_attn_blocksparse(p, ks, q.to(DEV), kd, vd, mask, o)
     torch.cuda.synchronize()
     L = cache_len(w.sides, ks)
-    _, units, ns = oracle.sparvar_units(w.sides, d, sink)
-    keep = oracle.sparvar_keep_mask(w.sides, d, ks, units, oracle.sparvar_select(A, ns, tau), sink)
     # one query of every 8x8 block of the 64x64 grid, plus the last
     rows = np.array(sorted({(8 * by + (by + bx) % 8) * 64 + 8 * bx + (3 * by) % 8
                             for by in range(8) for bx in range(8)} | {4095}), dtype=np.int64)
-    ref = oracle.attention_keep(q[:, :, torch.as_tensor(rows)].contiguous(), inp.k, inp.v, L, keep[rows])
+    ref = oracle.attention_keep(q[:, :, torch.as_tensor(rows)].contiguous(), inp.k, inp.v, L, ref_mask[rows])
     assert_close(o[:, :, torch.as_tensor(rows, device=DEV)], ref, "dynamic mask 1024px")
+    check_device_status()
+
+
+def test_exact_ties_go_to_the_lower_unit():
+    """q = 0: every key gets probability 1/L exactly, so units of equal size tie
+    exactly.  The fp32 bounds cannot order them; the fp64 re-score reproduces
+    the ties and the lower unit is taken first, as in the oracle."""
+    B, H, D, sink, d, ks = 1, 2, 64, 4, 6, 7                  # 32 x 32 decides 40 x 40
+    L = cache_len(SMALL, ks)
+    q_d = torch.zeros((B, H, SMALL[d] ** 2, D), dtype=torch.bfloat16)
+    k = randn_bf16((B, H, L, D), 1141)
+    p = V.problem(B, H, D, SMALL, kv_capacity=L)
+    A_ref = oracle.sparvar_scores(q_d, k, SMALL, d, sink)
+    for tau in (0.3, 0.61):
+        A, rs = gpu_scores(p, d, sink, tau, q_d.to(DEV), k.to(DEV))
+        assert np.all(rs == 1)                                # every block has ties at its cut
+        assert np.array_equal(A, A_ref)
+        got_mask, _ = gpu_mask(p, SMALL, d, ks, sink, A, tau)
+        assert np.array_equal(got_mask, oracle_mask(SMALL, d, ks, sink, A_ref, tau))
     check_device_status()
 
 
@@ -105,21 +155,22 @@ def test_dynamic_mask_head_dim_64_single_batch():
     v = randn_bf16((B, H, L, D), 1124)
     p = V.problem(B, H, D, SMALL, kv_capacity=L)
     kd, vd = k.to(DEV), v.to(DEV)
-    A = gpu_scores(p, d, sink, q_d.to(DEV), kd)
-    check_scores(A, oracle.sparvar_scores(q_d, k, SMALL, d, sink))
-    rp, en, sink_len = V.var_sparvar_mask_build(p, d, ks, sink, A, tau)
+    A, rs = gpu_scores(p, d, sink, tau, q_d.to(DEV), kd)
+    A_ref = oracle.sparvar_scores(q_d, k, SMALL, d, sink)
+    check_scores(A, rs, A_ref)
+    got_mask, (rp, en, sink_len) = gpu_mask(p, SMALL, d, ks, sink, A, tau)
+    ref_mask = oracle_mask(SMALL, d, ks, sink, A_ref, tau)
+    assert np.array_equal(got_mask, ref_mask)
     mask = V.block_mask_struct(8, torch.as_tensor(rp, device=DEV), torch.as_tensor(en, device=DEV), sink_len)
     o = torch.empty_like(q, device=DEV)
     V.var_attn_blocksparse(p, ks, q.to(DEV), kd, vd, mask, o)   # without a plan: the kernel merges the lists
     torch.cuda.synchronize()
-    _, units, ns = oracle.sparvar_units(SMALL, d, sink)
-    keep = oracle.sparvar_keep_mask(SMALL, d, ks, units, oracle.sparvar_select(A, ns, tau), sink)
-    assert_close(o, oracle.attention_keep(q, k, v, L, keep), "dynamic mask D 64")
+    assert_close(o, oracle.attention_keep(q, k, v, L, ref_mask), "dynamic mask D 64")
     check_device_status()
 
 
-def test_scores_two_passes_head_dim_128():
-    sides, sink, d = (1, 2, 4, 8, 16, 24, 32, 40, 48, 64), 4, 9        # 156 units > 128: two passes
+def test_scores_many_units_head_dim_128():
+    sides, sink, d = (1, 2, 4, 8, 16, 24, 32, 40, 48, 64), 4, 9        # 156 units
     B, H, D = 1, 1, 128
     L, N = cache_len(sides, d), sides[d] ** 2
     q = randn_bf16((B, H, N, D), 1131)
@@ -127,6 +178,11 @@ def test_scores_two_passes_head_dim_128():
     p = V.problem(B, H, D, sides)
     U, _ = V.var_sparvar_units(p, d, sink)
     assert U > 128
-    got = gpu_scores(p, d, sink, q.to(DEV), k.to(DEV))
-    check_scores(got, oracle.sparvar_scores(q, k, sides, d, sink))
+    A_ref = oracle.sparvar_scores(q, k, sides, d, sink)
+    for tau in (0.4, 0.85):
+        got, rs = gpu_scores(p, d, sink, tau, q.to(DEV), k.to(DEV))
+        check_scores(got, rs, A_ref)
+        for ks in (9,):
+            got_mask, _ = gpu_mask(p, sides, d, ks, sink, got, tau)
+            assert np.array_equal(got_mask, oracle_mask(sides, d, ks, sink, A_ref, tau))
     check_device_status()

@@ -83,8 +83,9 @@ _SIGS = {
     "var_attn_blocksparse": (C.c_int, [_PROB, C.c_int32, _P, _P, _P,
                                        C.POINTER(var_block_mask), _P, _P]),
     "var_sparvar_units": (C.c_int, [_PROB, C.c_int32, C.c_int32, _P, _P]),
-    "var_sparvar_workspace_bytes": (C.c_size_t, [_PROB, C.c_int32]),
-    "var_sparvar_scores": (C.c_int, [_PROB, C.c_int32, C.c_int32, _P, _P, _P, C.c_size_t, _P, _P]),
+    "var_sparvar_workspace_bytes": (C.c_size_t, [_PROB, C.c_int32, C.c_int32]),
+    "var_sparvar_scores": (C.c_int, [_PROB, C.c_int32, C.c_int32, C.c_double, C.c_int32, _P, _P, _P, C.c_size_t,
+                                     _P, _P, _P]),
     "var_sparvar_mask_build": (C.c_int, [_PROB, C.c_int32, C.c_int32, C.c_int32, _P, C.c_double, _P, _P,
                                          C.c_int32, _P, _P, _P]),
     "var_selftest_wait_timeout": (C.c_int, [C.c_int32, _P, _P]),
@@ -270,16 +271,22 @@ def var_sparvar_units(p: var_problem, decision_step: int, sink_max_side: int) ->
     return u.value, ns.value
 
 
-def var_sparvar_workspace_bytes(p: var_problem, decision_step: int) -> int:
-    return _lib.var_sparvar_workspace_bytes(C.byref(p), decision_step)
+VAR_SPARVAR_RESCORE_ALL = 1
 
 
-def var_sparvar_scores(p: var_problem, decision_step: int, sink_max_side: int, q: torch.Tensor, k: torch.Tensor,
-                       workspace: torch.Tensor, scores: torch.Tensor, stream=None) -> None:
-    """scores: device float64 [(side/8)^2, U]."""
+def var_sparvar_workspace_bytes(p: var_problem, decision_step: int, sink_max_side: int) -> int:
+    return _lib.var_sparvar_workspace_bytes(C.byref(p), decision_step, sink_max_side)
+
+
+def var_sparvar_scores(p: var_problem, decision_step: int, sink_max_side: int, tau: float, q: torch.Tensor,
+                       k: torch.Tensor, workspace: torch.Tensor, scores: torch.Tensor,
+                       rescored: Optional[torch.Tensor] = None, flags: int = 0, stream=None) -> None:
+    """scores: device float64 [(side/8)^2, U], exact enough to decide the selection at tau;
+    rescored: optional device int32 [(side/8)^2], 1 where a block was re-scored in fp64."""
     _check("var_sparvar_scores",
-           _lib.var_sparvar_scores(C.byref(p), decision_step, sink_max_side, _ptr(q), _ptr(k), _ptr(workspace),
-                                   workspace.numel() * workspace.element_size(), _ptr(scores), _stream(stream)))
+           _lib.var_sparvar_scores(C.byref(p), decision_step, sink_max_side, tau, flags, _ptr(q), _ptr(k),
+                                   _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(scores),
+                                   _ptr(rescored), _stream(stream)))
 
 
 def var_sparvar_mask_build(p: var_problem, decision_step: int, step: int, sink_max_side: int,

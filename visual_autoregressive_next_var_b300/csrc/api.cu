@@ -500,27 +500,35 @@ int var_sparvar_units(const var_problem* p, int32_t decision_step, int32_t sink_
     return VAR_OK;
 }
 
-size_t var_sparvar_workspace_bytes(const var_problem* p, int32_t decision_step)
+size_t var_sparvar_workspace_bytes(const var_problem* p, int32_t decision_step, int32_t sink_max_side)
 {
     StepGeom g;
     if (resolve(p, decision_step, &g)) return 0;
-    return varattn::sparvar_workspace_bytes(g);
+    varattn::UnitMap m;
+    if (build_unit_map(p, decision_step, sink_max_side, &m)) return 0;
+    return varattn::sparvar_workspace_bytes(g, m.U);
 }
 
-int var_sparvar_scores(const var_problem* p, int32_t decision_step, int32_t sink_max_side, const void* q,
-                       const void* k, void* workspace, size_t workspace_bytes, double* scores, void* stream)
+int var_sparvar_scores(const var_problem* p, int32_t decision_step, int32_t sink_max_side, double tau, int32_t flags,
+                       const void* q, const void* k, void* workspace, size_t workspace_bytes, double* scores,
+                       int32_t* rescored, void* stream)
 {
     StepGeom g;
     if (int rc = resolve(p, decision_step, &g)) return rc;
     varattn::UnitMap m;
     if (int rc = build_unit_map(p, decision_step, sink_max_side, &m)) return rc;
     if (!q || !k || !workspace || !scores) return VAR_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(scores) & 7))
+    if (!(tau >= 0.0 && tau <= 1.0) || (flags & ~VAR_SPARVAR_RESCORE_ALL)) return VAR_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+        (reinterpret_cast<uintptr_t>(scores) & 7) || (reinterpret_cast<uintptr_t>(rescored) & 3))
         return VAR_ERR_UNSUPPORTED;
-    int32_t* status = status_word(p);
-    if (!status) return VAR_ERR_CUDA;
-    return varattn::launch_sparvar_scores(g, m, q, k, workspace, workspace_bytes, scores,
-                                          static_cast<cudaStream_t>(stream), status);
+    if (workspace_bytes < varattn::sparvar_workspace_bytes(g, m.U)) return VAR_ERR_WORKSPACE;
+    // the fp64 softmax scale of the definition: 1/sqrt(head_dim) rounded once, or the caller's value
+    const double scale64 = p->softmax_scale == 0.f ? 1.0 / std::sqrt(static_cast<double>(p->head_dim))
+                                                   : static_cast<double>(p->softmax_scale);
+    return varattn::launch_sparvar_scores(g, m, q, k, tau, (flags & VAR_SPARVAR_RESCORE_ALL) ? 1 : 0, scale64,
+                                          workspace, workspace_bytes, scores, rescored,
+                                          static_cast<cudaStream_t>(stream));
 }
 
 int var_sparvar_mask_build(const var_problem* p, int32_t decision_step, int32_t step, int32_t sink_max_side,

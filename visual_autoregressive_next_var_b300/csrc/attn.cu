@@ -68,7 +68,7 @@ static TilePlan plan_tiles(int bh, int tiles_per_bh, int n_sms)
 template <int D, int MODE>
 static int launch_attn(const StepGeom& g, const void* q, const void* k, const void* v,
                        const int32_t* idx, int n_rows, void* o, cudaStream_t st, int32_t* status,
-                       bool halved = false, bool scatter = false, float* lse = nullptr, int v_cap = 0)
+                       bool halved = false, bool scatter = false, float* lse = nullptr)
 {
     using Lay = AttnLayout<D>;
     auto kern = attn_kernel<D, MODE, DenseMaps>;
@@ -91,10 +91,8 @@ static int launch_attn(const StepGeom& g, const void* q, const void* k, const vo
     {
         const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(g.L), BH};
         const uint64_t strides[2] = {D * 2ull, static_cast<uint64_t>(g.cap) * D * 2ull};
-        // V may have its own rows per (b,h) (a value tensor that is not the cache)
-        const uint64_t v_strides[2] = {D * 2ull, static_cast<uint64_t>(v_cap > 0 ? v_cap : g.cap) * D * 2ull};
         if (int rc = encode_tmap_bf16(&tk, k, 3, dims, strides, box)) return rc;
-        if (int rc = encode_tmap_bf16(&tv, v, 3, dims, v_strides, box)) return rc;
+        if (int rc = encode_tmap_bf16(&tv, v, 3, dims, strides, box)) return rc;
     }
     AttnArgs a = {};
     a.n_rows = n_rows;
@@ -126,17 +124,6 @@ int launch_attn_dense(const StepGeom& g, const void* q, const void* k, const voi
 {
     if (g.D == 128) return launch_attn<128, MODE_DENSE>(g, q, k, v, nullptr, g.N, o, st, status, false, false, lse);
     if (g.D == 64) return launch_attn<64, MODE_DENSE>(g, q, k, v, nullptr, g.N, o, st, status, false, false, lse);
-    return VAR_ERR_UNSUPPORTED;
-}
-
-int launch_attn_dense_vcap(const StepGeom& g, const void* q, const void* k, const void* v, int v_cap, void* o,
-                           cudaStream_t st, int32_t* status)
-{
-    if (v_cap < g.L) return VAR_ERR_INVALID_ARG;
-    if (g.D == 128)
-        return launch_attn<128, MODE_DENSE>(g, q, k, v, nullptr, g.N, o, st, status, false, false, nullptr, v_cap);
-    if (g.D == 64)
-        return launch_attn<64, MODE_DENSE>(g, q, k, v, nullptr, g.N, o, st, status, false, false, nullptr, v_cap);
     return VAR_ERR_UNSUPPORTED;
 }
 

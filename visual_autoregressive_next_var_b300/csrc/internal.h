@@ -53,9 +53,6 @@ int encode_tmap_bf16(CUtensorMap* out, const void* base, int rank, const uint64_
 // Launchers: `status` is the device status word of the call.
 int launch_attn_dense(const StepGeom& g, const void* q, const void* k, const void* v, void* o,
                       cudaStream_t st, int32_t* status, float* lse = nullptr);
-// As launch_attn_dense with V read at its own stride of v_cap rows per (b,h).
-int launch_attn_dense_vcap(const StepGeom& g, const void* q, const void* k, const void* v, int v_cap, void* o,
-                           cudaStream_t st, int32_t* status);
 int launch_attn_pruned(const StepGeom& g, const void* q, const void* k, const void* v,
                        const int32_t* idx, int keep_k, void* o, cudaStream_t st, int32_t* status, bool scatter);
 int launch_attn_dense_halved(const StepGeom& g, const void* q, const void* k, const void* v, void* o,
@@ -83,11 +80,15 @@ struct UnitMap {
     int side[VAR_MAX_SCALES];
     int ubase[VAR_MAX_SCALES];   // its first unit
 };
-size_t sparvar_workspace_bytes(const StepGeom& g);
+size_t sparvar_workspace_bytes(const StepGeom& g, int U);
 // One-thread kernel whose wait gives up after limit_us and records VAR_ERR_TIMEOUT.
 int launch_wait_timeout(int limit_us, cudaStream_t st, int32_t* status);
-int launch_sparvar_scores(const StepGeom& g, const UnitMap& m, const void* q, const void* k, void* ws,
-                          size_t ws_bytes, double* scores, cudaStream_t st, int32_t* status);
+// Block scores of the decision step, exact enough to decide the selection at
+// tau as the fp64 definition does (certified fp32, fp64 re-score of unsettled
+// blocks; force: re-score every block).  scale64: the softmax scale in fp64.
+int launch_sparvar_scores(const StepGeom& g, const UnitMap& m, const void* q, const void* k, double tau, int force,
+                          double scale64, void* ws, size_t ws_bytes, double* scores, int32_t* rescored,
+                          cudaStream_t st);
 int launch_restore_scatter(int B, int H, int D, int sp, int s, const void* prev, const void* oc,
                            const int32_t* idx, int keep_k, void* out, cudaStream_t st, int32_t* status,
                            bool fill_only);
