@@ -61,6 +61,23 @@ int sm_count()
     return cache[dev];
 }
 
+long long l2_bytes()
+{
+    static std::mutex mu;
+    static long long cache[64] = {};
+    int dev = 0;
+    if (current_device(&dev) != cudaSuccess) return 0;
+    int n = 0;
+    if (rt_mocked())
+        return rt().device_attribute(&n, cudaDevAttrL2CacheSize, dev) == cudaSuccess && n > 0 ? n : 0;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!cache[dev]) {
+        if (rt().device_attribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess || n <= 0) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
 int encode_tmap_bf16(CUtensorMap* out, const void* base, int rank, const uint64_t* dims,
                      const uint64_t* strides_bytes, const uint32_t* box)
 {

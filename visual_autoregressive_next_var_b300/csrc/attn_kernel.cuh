@@ -130,8 +130,10 @@ struct AttnArgs {
     const int32_t* entries; // packed (scale << 24) | (u << 12) | v
     const int32_t* sq_ptr;  // optional host-built plan: units of square q
     const int2* sq_units;
-    const int32_t* sq_order;// squares in the order CTAs take them (all heads of one square together)
+    const int32_t* sq_order;// squares in the order CTAs take them (heaviest first)
     int32_t n_bh;           // B * H
+    int32_t head_group;     // planned order: heads per group (1 .. n_bh); groups run one after the
+                            // other, inside a group the squares in sq_order, all its heads together
     int32_t plan_units;     // entries of sq_units
     int32_t sides[VAR_MAX_SCALES];
 };
@@ -324,9 +326,15 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
     if constexpr (SPARSE) {
         const int nsq2 = args.nsq * args.nsq;
         int sq;
-        if (args.sq_order) {              // planned: square-major, heaviest squares first
-            const int rnk = blockIdx.x / args.n_bh;
-            bh = blockIdx.x - rnk * args.n_bh;
+        if (args.sq_order) {
+            // planned: head groups in turn (their K/V stay in L2 while the group
+            // runs); inside a group the squares heaviest first, all its heads together
+            const int G = args.head_group;
+            const int g = blockIdx.x / (G * nsq2);
+            const int o = blockIdx.x - g * G * nsq2;
+            const int gs = min(G, args.n_bh - g * G);
+            const int rnk = o / gs;
+            bh = g * G + (o - rnk * gs);
             sq = min(max(__ldg(args.sq_order + rnk), 0), nsq2 - 1);
         } else {
             bh = blockIdx.x / nsq2;

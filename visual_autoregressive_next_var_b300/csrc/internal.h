@@ -97,5 +97,7 @@ inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? VAR_OK : VAR_E
 
 // SM count of the current device (0 if it cannot be read).
 int sm_count();
+// L2 cache bytes of the current device (0 if it cannot be read).
+long long l2_bytes();
 
 }  // namespace varattn

@@ -53,7 +53,7 @@ const CudaOps kReal = {cudaGetDevice,          cudaDeviceGetAttribute, real_get_
                        real_encode_tiled};
 
 // ---------------------------------------------------------------- mock
-// A fake device 0 with 148 SMs.  Each call counts; the call whose count equals
+// A fake device 0 with 148 SMs and 126 MB of L2.  Each call counts; the call whose count equals
 // the requested one fails.  Symbol addresses point at a host buffer that only
 // the mock's own memcpy touches; launches run nothing.
 
@@ -74,10 +74,10 @@ cudaError_t mock_get_device(int* d)
     *d = 0;
     return cudaSuccess;
 }
-cudaError_t mock_device_attribute(int* v, cudaDeviceAttr, int)
+cudaError_t mock_device_attribute(int* v, cudaDeviceAttr a, int)
 {
     if (mock_fail()) return cudaErrorInvalidValue;
-    *v = 148;
+    *v = a == cudaDevAttrL2CacheSize ? 126 * 1024 * 1024 : 148;
     return cudaSuccess;
 }
 cudaError_t mock_get_symbol_address(void** p, const void*)
