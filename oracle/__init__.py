@@ -176,9 +176,14 @@ def top_k_ascending(values: np.ndarray, keep_k: int) -> np.ndarray:
 def guided_pivot(sal: np.ndarray, side: int, keep_k: int):
     """ARVAR attention-guided pivots: the head and query mean of the per-head
     saliency sums [B, H, N'], bilinearly upsampled to side x side, Top-K.
+    The heads are added one at a time in order, in fp64 (a fixed order, so the
+    rounding is defined), then divided by H N'.
     Returns (idx [B, K] ascending, values [B, side*side])."""
     B, H, Np = sal.shape
-    v = bilinear_map(sal.sum(axis=1) / (H * Np), side)
+    acc = np.zeros((B, Np), dtype=np.float64)
+    for h in range(H):
+        acc += sal[:, h, :]
+    v = bilinear_map(acc / (H * Np), side)
     return top_k_ascending(v, keep_k), v
 
 

@@ -96,6 +96,33 @@ def test_top_k_ascending_ties_and_order():
     assert np.array_equal(idx, [[0, 1, 2, 3, 4]] * 2) and np.allclose(vals, 1.0 / 4)
 
 
+def test_guided_pivot_values_follow_the_stated_order():
+    """The interpolated values are the head sum (heads added in order), divided
+    by H N', then the bilinear formula term by term: bit for bit equal to the
+    same operations on Python floats."""
+    sal = np.random.default_rng(7).random((2, 3, 16))
+    sp, s = 4, 6
+    _, v = oracle.guided_pivot(sal, s, 5)
+    for b in range(2):
+        m = []
+        for j in range(16):
+            acc = 0.0
+            for h in range(3):
+                acc += float(sal[b, h, j])
+            m.append(acc / (3 * 16))
+        for y in range(s):
+            for x in range(s):
+                def ax(d):
+                    src = max((d + 0.5) * sp / s - 0.5, 0.0)
+                    i0 = min(int(np.floor(src)), sp - 1)
+                    return i0, min(i0 + 1, sp - 1), src - i0
+                y0, y1, ly = ax(y)
+                x0, x1, lx = ax(x)
+                top = m[y0 * sp + x0] * (1 - lx) + m[y0 * sp + x1] * lx
+                bot = m[y1 * sp + x0] * (1 - lx) + m[y1 * sp + x1] * lx
+                assert v[b, y * s + x] == top * (1 - ly) + bot * ly
+
+
 def test_branch_halved_attention_repeats_the_conditional_half():
     # the conditional half is the plain attention of those batch elements; the
     # unconditional half carries the same values, whatever its own inputs
