@@ -324,42 +324,45 @@ __global__ void __cluster_dims__(kSlabs, 1, 1) __launch_bounds__(kSumThreads)
         p[e] += __shfl_xor_sync(0xffffffffu, p[e], 16);
         q[e] += __shfl_xor_sync(0xffffffffu, q[e], 16);
     }
-    long long* red = reinterpret_cast<long long*>(ring);    // [warps][kChunk][2], the ring is idle now
+    // lanes < 16 hold a warp's partial sums: entry (warp, e, segment) of 16 bytes,
+    // so a warp's stores of one e are contiguous (no bank conflicts)
+    static_assert(kSegs == 16, "two row groups per warp");
+    longlong2* red = reinterpret_cast<longlong2*>(ring);    // [warps][8][16], the ring is idle now
     const int warp = tid >> 5, lane = tid & 31;
     if (lane < 16) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            red[(warp * kChunk + seg * 8 + e) * 2] = p[e];
-            red[(warp * kChunk + seg * 8 + e) * 2 + 1] = q[e];
-        }
+        for (int e = 0; e < 8; ++e) red[(warp * 8 + e) * 16 + seg] = make_longlong2(p[e], q[e]);
     }
     __syncthreads();
     if (tid < kChunk) {
+        // thread (e, segment) = (tid / 16, tid % 16): channel segment*8 + e, summed over the warps
+        const int e = tid >> 4, sg = tid & 15;
         long long sp = 0, sq = 0;
 #pragma unroll
         for (int w = 0; w < kSumThreads / 32; ++w) {
-            sp += red[(w * kChunk + tid) * 2];
-            sq += red[(w * kChunk + tid) * 2 + 1];
+            const longlong2 v = red[(w * 8 + e) * 16 + sg];
+            sp += v.x;
+            sq += v.y;
         }
-        part[tid][0] = sp;
-        part[tid][1] = sq;
+        part[sg * 8 + e][0] = sp;
+        part[sg * 8 + e][1] = sq;
     }
     cluster_sync_all();
-    // CTA `rank` finishes channels [rank*16, rank*16 + 16) of the chunk
+    // CTA `rank` finishes channels [rank*kPer, rank*kPer + kPer) of the chunk: thread
+    // (channel, peer) = (tid / 8, tid % 8) reads one peer's partial sums, the
+    // eight lanes of a channel add them
     constexpr int kPer = kChunk / kSlabs;
-    if (tid < kPer) {
-        const int cl = rank * kPer + tid;
+    if (tid < kPer * kSlabs) {
+        const int cl = rank * kPer + (tid >> 3);
         const int cc = chunk * kChunk + cl;
-        long long sp = 0, sq = 0;
-        const uint32_t la = smem_u32(&part[cl][0]);
+        long long sp, sq;
+        ld_peer_pair(smem_u32(&part[cl][0]), static_cast<uint32_t>(tid & 7), sp, sq);
 #pragma unroll
-        for (int k = 0; k < kSlabs; ++k) {
-            long long a, bq;
-            ld_peer_pair(la, static_cast<uint32_t>(k), a, bq);
-            sp += a;
-            sq += bq;
+        for (int off = 1; off < kSlabs; off <<= 1) {
+            sp += __shfl_xor_sync(0xffffffffu, sp, off);
+            sq += __shfl_xor_sync(0xffffffffu, sq, off);
         }
-        if (cc < C) {
+        if ((tid & 7) == 0 && cc < C) {
             const __int128 t = static_cast<__int128>(sp) * (static_cast<__int128>(1) << 36) + static_cast<__int128>(sq);
             const double s = i128_to_f64_rn(t) * 0x1p-60;     // exact power-of-two scaling
             const double m = __ddiv_rn(s, static_cast<double>(N));
