@@ -522,13 +522,18 @@ def extra_rows(V, dev, step: Step, inp, iters: int, peaks, host_bytes):
     t_sel = time_graph(lambda: V.var_guided_pivot_select(p, FINAL, src, sal, step.K[FINAL], gidx, gws),
                        iters, flush)
     L_src = cache_len(WORKLOADS[W1024].sides, src)
+    gx_ws = torch.empty(V.var_guided_pivot_exact_workspace_bytes(p, FINAL, src), dtype=torch.uint8, device=dev)
+    t_exact = time_graph(lambda: V.var_guided_pivot_select_exact(p, FINAL, src, q_src, step.k, step.K[FINAL], gidx,
+                                                                 gx_ws), max(3, iters // 4), flush)
     fl_sal = 2.0 * B * H * Ns * Ns * D            # S^T = K_self Q^T
     rows["guided_pivot_from_32x32"] = {
         "ms": t_sal + t_sel, "saliency_ms": t_sal, "select_ms": t_sel,
         "saliency_TFLOP/s": fl_sal / t_sal / 1e9,
         "source_dense_ms": t_plain, "source_dense_with_lse_ms": t_lse,
+        "exact_fp64_ms": t_exact,
         "note": f"source step 32x32 ({Ns} queries, {L_src} keys) -> 64x64, keep 1/5; the row "
-                "statistics are written by the source step's own dense attention",
+                "statistics are written by the source step's own dense attention; exact_fp64_ms: the "
+                "ranking decided in fp64 (var_guided_pivot_select_exact, from the source queries and keys)",
         "timing": "CUDA graph replay after an L2 flush"}
     # SparVAR dynamic pattern: the 32x32 step's block scores decide the 64x64 step's mask
     d_sv, tau_sv = src, 0.8

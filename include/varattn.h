@@ -244,6 +244,34 @@ VAR_API int var_guided_pivot_select(const var_problem* p, int32_t step, int32_t 
                                     int32_t keep_k, int32_t* idx, float* scores, void* workspace,
                                     size_t workspace_bytes, void* stream);
 
+/* Bytes of device workspace var_guided_pivot_select_exact needs (0 on invalid arguments). */
+VAR_API size_t var_guided_pivot_exact_workspace_bytes(const var_problem* p, int32_t step, int32_t src_step);
+
+/*
+ * Attention-guided pivot selection ("ARVAR" Key Design 2) decided in fp64: the
+ * same values as var_attn_saliency + var_guided_pivot_select describe, but
+ * evaluated from the source step's queries and keys in fp64 on the device in
+ * the definition's own order -- scores q.k summed over channels in order, the
+ * softmax denominator over the L' keys added in key order, each token's
+ * saliency added over the source queries in order, the head sum in head order,
+ * divided by H N', the bilinear formula term by term -- and ranked exactly on
+ * those values (equal values: lower flat index first).  Use it where the kept
+ * set must equal the fp64 definition's; var_guided_pivot_select ranks fp32
+ * values and is three orders of magnitude faster (fp64 runs at a small
+ * fraction of the fp32 rate on B300).  Only two values closer than the last
+ * bit of a double exp can still be ordered differently from a CPU evaluation.
+ * q_src: [B][H][side[src_step]^2][D]; k: [B][H][kv_capacity][D] (the cache, at
+ * least the source step's L' rows); idx: [B][keep_k] int32, ascending; values:
+ * optional [B][side[step]^2] fp64 (the interpolated values) or NULL; workspace
+ * of var_guided_pivot_exact_workspace_bytes() bytes, 256-byte aligned.
+ * Errors: VAR_ERR_INVALID_ARG (src_step >= step, keep_k out of range, null
+ * pointers), VAR_ERR_UNSUPPORTED (alignment, a target grid over ~20,000
+ * tokens), VAR_ERR_WORKSPACE, VAR_ERR_CUDA.
+ */
+VAR_API int var_guided_pivot_select_exact(const var_problem* p, int32_t step, int32_t src_step, const void* q_src,
+                                          const void* k, int32_t keep_k, int32_t* idx, double* values,
+                                          void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * Dense attention under Branch Halving ("ARVAR" Key Design 1: at a selected
  * step only the conditional branch goes through the block and its output is

@@ -33,6 +33,7 @@ def _cases(V):
     p64 = V.problem(1, 3, 64, sides)
     ws_piv = L.var_pivot_workspace_bytes(C.byref(p), 9, 256)
     ws_gd = L.var_guided_pivot_workspace_bytes(C.byref(p), 9)
+    ws_gx = L.var_guided_pivot_exact_workspace_bytes(C.byref(p), 9, 8)
     ws_sv = L.var_sparvar_workspace_bytes(C.byref(p), 9, 16)
     m = V.var_block_mask()
     m.qblock_side, m.n_qblocks, m.sink_len, m.nnz = 8, 16, 521, 64
@@ -57,6 +58,8 @@ def _cases(V):
         ("var_attn_saliency", lambda: L.var_attn_saliency(C.byref(p), 8, f, f, f, f, None)),
         ("var_guided_pivot_select", lambda: L.var_guided_pivot_select(C.byref(p), 9, 8, f, 204, f, None, f, ws_gd,
                                                                       None)),
+        ("var_guided_pivot_select_exact", lambda: L.var_guided_pivot_select_exact(C.byref(p), 9, 8, f, f, 204, f, f,
+                                                                                  f, ws_gx, None)),
         ("var_attn_blocksparse", lambda: L.var_attn_blocksparse(C.byref(p), 9, f, f, f, C.byref(m), f, None)),
         ("var_attn_blocksparse_plan", lambda: L.var_attn_blocksparse(C.byref(p), 9, f, f, f, C.byref(mp), f, None)),
         ("var_sparvar_scores", lambda: L.var_sparvar_scores(C.byref(p), 9, 16, 0.8, 0, f, f, f, ws_sv, f, fs, None)),

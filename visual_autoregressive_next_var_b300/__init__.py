@@ -71,6 +71,9 @@ _SIGS = {
     "var_attn_pruned_scatter": (C.c_int, [_PROB, C.c_int32, _P, _P, _P, _P, C.c_int32, _P, _P]),
     "var_restore_fill": (C.c_int, [_PROB, C.c_int32, _P, _P, C.c_int32, _P, _P]),
     "var_attn_dense_halved": (C.c_int, [_PROB, C.c_int32, _P, _P, _P, _P, _P]),
+    "var_guided_pivot_exact_workspace_bytes": (C.c_size_t, [_PROB, C.c_int32, C.c_int32]),
+    "var_guided_pivot_select_exact": (C.c_int, [_PROB, C.c_int32, C.c_int32, _P, _P, C.c_int32, _P, _P, _P,
+                                                C.c_size_t, _P]),
     "var_attn_dense_lse": (C.c_int, [_PROB, C.c_int32, _P, _P, _P, _P, _P, _P]),
     "var_attn_saliency": (C.c_int, [_PROB, C.c_int32, _P, _P, _P, _P, _P]),
     "var_guided_pivot_workspace_bytes": (C.c_size_t, [_PROB, C.c_int32]),
@@ -250,6 +253,20 @@ def var_guided_pivot_select(p: var_problem, step: int, src_step: int, sal: torch
            _lib.var_guided_pivot_select(C.byref(p), step, src_step, _ptr(sal), keep_k, _ptr(idx), _ptr(scores),
                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
                                         _stream(stream)))
+
+
+def var_guided_pivot_exact_workspace_bytes(p: var_problem, step: int, src_step: int) -> int:
+    return _lib.var_guided_pivot_exact_workspace_bytes(C.byref(p), step, src_step)
+
+
+def var_guided_pivot_select_exact(p: var_problem, step: int, src_step: int, q_src: torch.Tensor, k: torch.Tensor,
+                                  keep_k: int, idx: Optional[torch.Tensor], workspace: torch.Tensor,
+                                  values: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Attention-guided pivots ranked on fp64 values evaluated in the definition's order."""
+    _check("var_guided_pivot_select_exact",
+           _lib.var_guided_pivot_select_exact(C.byref(p), step, src_step, _ptr(q_src), _ptr(k), keep_k, _ptr(idx),
+                                              _ptr(values), _ptr(workspace),
+                                              workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def var_workspace_bytes(p: var_problem, step: int, channels: int, keep_k: int) -> int:

@@ -10,7 +10,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libvarattn.so")
-SOURCES = ["rt.cu", "api.cu", "attn.cu", "blocksparse.cu", "pivot.cu", "restore.cu", "saliency.cu", "sparvar.cu", "selftest.cu"]
+SOURCES = ["rt.cu", "api.cu", "attn.cu", "blocksparse.cu", "pivot.cu", "restore.cu", "saliency.cu", "guided_exact.cu", "sparvar.cu", "selftest.cu"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",

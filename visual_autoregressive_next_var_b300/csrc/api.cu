@@ -276,6 +276,33 @@ int var_guided_pivot_select(const var_problem* p, int32_t step, int32_t src_step
                                workspace_bytes, static_cast<cudaStream_t>(stream), status);
 }
 
+size_t var_guided_pivot_exact_workspace_bytes(const var_problem* p, int32_t step, int32_t src_step)
+{
+    StepGeom g, gs;
+    if (resolve(p, step, &g) != VAR_OK || src_step < 0 || src_step >= step || resolve(p, src_step, &gs) != VAR_OK)
+        return 0;
+    return guided_exact_workspace_bytes(g.B * g.H, gs.N);
+}
+
+int var_guided_pivot_select_exact(const var_problem* p, int32_t step, int32_t src_step, const void* q_src,
+                                  const void* k, int32_t keep_k, int32_t* idx, double* values, void* workspace,
+                                  size_t workspace_bytes, void* stream)
+{
+    StepGeom g, gs;
+    if (int rc = resolve(p, step, &g)) return rc;
+    if (src_step < 0 || src_step >= step) return VAR_ERR_INVALID_ARG;
+    if (int rc = resolve(p, src_step, &gs)) return rc;
+    if (!q_src || !k || keep_k < 0 || keep_k > g.N || (keep_k > 0 && !idx)) return VAR_ERR_INVALID_ARG;
+    if (!aligned16(q_src) || !aligned16(k) || (reinterpret_cast<uintptr_t>(values) & 7)) return VAR_ERR_UNSUPPORTED;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+        workspace_bytes < guided_exact_workspace_bytes(g.B * g.H, gs.N))
+        return VAR_ERR_WORKSPACE;
+    const double scale64 = p->softmax_scale == 0.f ? 1.0 / std::sqrt(static_cast<double>(p->head_dim))
+                                                   : static_cast<double>(p->softmax_scale);
+    return launch_guided_exact(gs, g.B, g.H, g.side, q_src, k, scale64, keep_k, idx, values, workspace,
+                               workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
 int var_attn_dense_halved(const var_problem* p, int32_t step, const void* q, const void* k, const void* v,
                           void* o, void* stream)
 {

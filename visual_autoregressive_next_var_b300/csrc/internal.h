@@ -68,6 +68,10 @@ int launch_select_exact(int B, int N, int keep_k, const float* keys_lo, const fl
 int launch_saliency(const StepGeom& g, int n_src, int L_src, const void* q, const void* k, const float* lse,
                     float* sal, cudaStream_t st, int32_t* status);
 size_t guided_workspace_bytes(int B, int N);
+// Attention-guided pivots decided in fp64 (guided_exact.cu): g_src is the source step.
+size_t guided_exact_workspace_bytes(int BH, int Np);
+int launch_guided_exact(const StepGeom& g_src, int B, int H, int s, const void* q_src, const void* k, double scale64,
+                        int keep_k, int32_t* idx, double* values, void* ws, size_t ws_bytes, cudaStream_t st);
 int launch_guided_pivot(int B, int H, int sp, int s, const float* sal, int keep_k, int32_t* idx, float* scores,
                         void* ws, size_t ws_bytes, cudaStream_t st, int32_t* status);
 // The decision step's 64-key units (dynamic sparse pattern): the sink range
