@@ -20,7 +20,8 @@ import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libvarattn.so")
+# VARATTN_DEBUG=1 loads the debug build (device-side input checks, see build.py --debug)
+LIB_PATH = os.path.join(_HERE, "libvarattn_debug.so" if os.environ.get("VARATTN_DEBUG") == "1" else "libvarattn.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "varattn.h")
 TEST_HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "varattn_test.h")
 MAX_SCALES = 32
@@ -55,7 +56,7 @@ class var_block_mask(C.Structure):
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build the CUDA library first "
-                      "(python visual_autoregressive_next_var_b300/build.py)")
+                      "(python visual_autoregressive_next_var_b300/build.py [--debug])")
 _lib = C.CDLL(LIB_PATH)
 
 _P = C.c_void_p

@@ -194,6 +194,7 @@ int var_attn_pruned(const var_problem* p, int32_t step, const void* q, const voi
         return VAR_ERR_UNSUPPORTED;
     int32_t* status = status_word(p);
     if (!status) return VAR_ERR_CUDA;
+    VAR_DEBUG_CHECK_INDICES(idx, g.B, keep_k, g.N, false, status, static_cast<cudaStream_t>(stream));
     return launch_attn_pruned(g, q, k, v, idx, keep_k, o_compact, static_cast<cudaStream_t>(stream), status,
                               false);
 }
@@ -209,6 +210,7 @@ int var_attn_pruned_scatter(const var_problem* p, int32_t step, const void* q, c
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return VAR_ERR_UNSUPPORTED;
     int32_t* status = status_word(p);
     if (!status) return VAR_ERR_CUDA;
+    VAR_DEBUG_CHECK_INDICES(idx, g.B, keep_k, g.N, true, status, static_cast<cudaStream_t>(stream));
     return launch_attn_pruned(g, q, k, v, idx, keep_k, out, static_cast<cudaStream_t>(stream), status, true);
 }
 
@@ -223,6 +225,7 @@ int var_restore_fill(const var_problem* p, int32_t step, const void* prev, const
     if (!aligned16(prev) || !aligned16(out)) return VAR_ERR_UNSUPPORTED;
     int32_t* status = status_word(p);
     if (!status) return VAR_ERR_CUDA;
+    VAR_DEBUG_CHECK_INDICES(idx, g.B, keep_k, g.N, true, status, static_cast<cudaStream_t>(stream));
     return launch_restore_scatter(g.B, g.H, g.D, p->side[step - 1], g.side, prev, nullptr, idx, keep_k, out,
                                   static_cast<cudaStream_t>(stream), status, true);
 }
@@ -328,6 +331,7 @@ int var_restore_scatter(const var_problem* p, int32_t step, const void* prev, co
         return VAR_ERR_UNSUPPORTED;
     int32_t* status = status_word(p);
     if (!status) return VAR_ERR_CUDA;
+    VAR_DEBUG_CHECK_INDICES(idx, g.B, keep_k, g.N, true, status, static_cast<cudaStream_t>(stream));
     return launch_restore_scatter(g.B, g.H, g.D, p->side[step - 1], g.side, prev, o_compact, idx,
                                   keep_k, out, static_cast<cudaStream_t>(stream), status, false);
 }

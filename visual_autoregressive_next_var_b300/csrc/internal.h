@@ -99,6 +99,20 @@ int launch_restore_scatter(int B, int H, int D, int sp, int s, const void* prev,
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? VAR_OK : VAR_ERR_CUDA; }
 
+#ifdef VAR_DEBUG
+// Debug build: check an index list on the device (entries in [0, N), strictly
+// ascending per batch element if asked); a bad list records VAR_ERR_INVALID_ARG.
+int debug_check_indices(const int32_t* idx, int B, int K, int N, bool ascending, int32_t* status, cudaStream_t st);
+#define VAR_DEBUG_CHECK_INDICES(idx, B, K, N, asc, status, st)                                  \
+    do {                                                                                        \
+        if (int rc_ = debug_check_indices((idx), (B), (K), (N), (asc), (status), (st))) return rc_; \
+    } while (0)
+#else
+#define VAR_DEBUG_CHECK_INDICES(idx, B, K, N, asc, status, st) \
+    do {                                                       \
+    } while (0)
+#endif
+
 // SM count of the current device (0 if it cannot be read).
 int sm_count();
 // L2 cache bytes of the current device (0 if it cannot be read).
