@@ -67,8 +67,8 @@ LAUNCHES_PER_STEP = 12               # dense 1, (pivot 3, pruned 1, restore 1) x
 KERNEL_NAMES = {"attn_dense_1024px": "attn_kernel<128, dense>", "attn_pruned_48": "attn_kernel<128, gather>",
                 "attn_pruned_64": "attn_kernel<128, gather>", "attn_blocksparse_2k": "attn_kernel<128, sparse>",
                 "pivot_select_48": "pivot kernels", "pivot_select_64": "pivot kernels",
-                "restore_scatter_40to48": "restore_scatter_kernel<128>",
-                "restore_scatter_48to64": "restore_scatter_kernel<128>"}
+                "restore_scatter_40to48": "restore_rows_kernel<128>",
+                "restore_scatter_48to64": "restore_rows_kernel<128>"}
 TRAFFIC_KEYS = {"attn_dense_1024px": "attn_kernel<128, dense>:dense_1024px_final",
                 "attn_blocksparse_2k": "attn_kernel<128, sparse>:blocksparse_2k_final",
                 "attn_pruned_64": "attn_kernel<128, gather>:pruned_64x64_k819"}
