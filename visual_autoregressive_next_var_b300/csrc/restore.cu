@@ -4,13 +4,15 @@
 // the kept rows.
 //
 // Scatter mode: restore_rows_kernel, one CTA per output grid row y and (b, h).
-// The two source rows y0, y1 of prev (2 x s' tokens) are staged in shared
-// memory with cp.async; while they are in flight two warps find the slice of
-// the ascending index list that falls in row y (32-ary searches: all lanes
-// probe at once, one load round per factor of 32 of the list's length) and the
-// kept rows of o_compact named by the slice are staged too.  Every output
-// token of the row is then either its staged o_compact row (kept) or a blend of
-// four staged taps, written with 16-byte stores: each row of out written once.
+// One thread issues two bulk copies (cp.async.bulk, completion on an mbarrier)
+// of the source rows y0, y1 of prev (2 x s' tokens, contiguous) into shared
+// memory.  Meanwhile the CTA finds the kept tokens of row y: index lists of up
+// to 4,096 entries are read whole (one coalesced pass, every entry in the row
+// marks its token), longer ones by two 32-ary searches for the row's slice.
+// The kept tokens are copied from o_compact straight away (they need no
+// source row); once the source rows have landed every other token is the
+// blend of four staged taps.  Every row of out is written once, with 16-byte
+// stores.
 //
 // Fill mode (the kept rows are written by the in-place pruned attention, maybe
 // concurrently, so they must not be touched): fill_rows_kernel, one CTA per 64
@@ -29,12 +31,6 @@ constexpr int kFillTok = 64;
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-
 
 // Source coordinate of output pixel d of an axis from an n_in-wide one
 // (half-pixel centres, clamped to 0; ratio = n_in / n_out): taps i0, i1 and
@@ -90,65 +86,88 @@ __device__ __forceinline__ int warp_lower_bound(const int32_t* a, int n, int key
 
 // ------------------------------------------------------------------ scatter mode
 
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+constexpr int kScanMax = 4096;   // index lists up to this length are read whole by every CTA
+
 template <int D>
 __global__ void __launch_bounds__(256)
     restore_rows_kernel(const __nv_bfloat16* __restrict__ prev, const __nv_bfloat16* __restrict__ oc,
                         const int32_t* __restrict__ idx, int keep_k, __nv_bfloat16* __restrict__ out, int H, int sp,
                         int s, float ratio, int32_t* status)
 {
-    constexpr int LPT = D / 8;              // 16-byte groups per token row
-    // [2][sp][LPT] source rows y0, y1, then [s][LPT] kept rows of o_compact, then [s] int
-    extern __shared__ __align__(16) uint4 stage[];
+    constexpr int LPT = D / 8;
+    extern __shared__ __align__(128) uint4 stage[];       // [2][sp][LPT] source rows y0, y1, then [s] int
+    __shared__ __align__(8) uint64_t full;
     __shared__ int range[2];
     const int y = blockIdx.x, bh = blockIdx.y, b = bh / H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int per_row = sp * LPT;
-    uint4* kst = stage + 2 * per_row;
-    int* slot = reinterpret_cast<int*>(kst + s * LPT);   // token x -> staged kept row, or -1
+    int* slot = reinterpret_cast<int*>(stage + 2 * per_row);
     int y0, y1;
     float ly;
     axis_taps(y, ratio, sp, y0, y1, ly);
     const uint4* P = reinterpret_cast<const uint4*>(prev + static_cast<size_t>(bh) * sp * sp * D);
-    for (int e = threadIdx.x; e < 2 * per_row; e += blockDim.x) {
-        const int r = e / per_row, o = e - r * per_row;
-        cp_async16(smem_u32(stage + e), P + static_cast<size_t>(r ? y1 : y0) * per_row + o);
+    const uint32_t bar = smem_u32(&full);
+    const uint32_t row_bytes = static_cast<uint32_t>(per_row) * 16u;
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, (y1 != y0 ? 2u : 1u) * row_bytes);
+        bulk_g2s(smem_u32(stage), P + static_cast<size_t>(y0) * per_row, row_bytes, bar);
+        if (y1 != y0) bulk_g2s(smem_u32(stage + per_row), P + static_cast<size_t>(y1) * per_row, row_bytes, bar);
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
     for (int x = threadIdx.x; x < s; x += blockDim.x) slot[x] = -1;
     const int32_t* ib = idx + static_cast<size_t>(b) * keep_k;
-    if (warp < 2) {
-        const int r = keep_k ? warp_lower_bound(ib, keep_k, (y + warp) * s) : 0;
+    const int lo = y * s;
+    if (keep_k > kScanMax && warp < 2) {
+        const int r = warp_lower_bound(ib, keep_k, lo + warp * s);
         if (lane == 0) range[warp] = r;
     }
     __syncthreads();
-    // kept tokens of this row: idx[j0, j0 + nk); more than s means the list is
-    // not strictly ascending (reported, and cut to the row's s tokens)
-    const int j0 = range[0], nk = min(range[1] - range[0], s);
-    if (threadIdx.x == 0 && range[1] - range[0] > s) atomicCAS(status, 0, VAR_ERR_INVALID_ARG);
-    for (int t = threadIdx.x; t < nk; t += blockDim.x) {
-        const int x = __ldg(ib + j0 + t) - y * s;          // in [0, s) for an ascending list
-        if (x >= 0 && x < s) slot[x] = t;
+    if (keep_k <= kScanMax) {
+        for (int j = threadIdx.x; j < keep_k; j += blockDim.x) {
+            const int t = __ldg(ib + j) - lo;
+            if (t >= 0 && t < s) slot[t] = j;
+        }
+    } else {
+        const int j0 = range[0], nk = min(range[1] - range[0], s);
+        if (threadIdx.x == 0 && range[1] - range[0] > s) atomicCAS(status, 0, VAR_ERR_INVALID_ARG);
+        for (int t = threadIdx.x; t < nk; t += blockDim.x) {
+            const int x = __ldg(ib + j0 + t) - lo;
+            if (x >= 0 && x < s) slot[x] = j0 + t;
+        }
     }
-    const uint4* Cp = reinterpret_cast<const uint4*>(oc + (static_cast<size_t>(bh) * keep_k + j0) * D);
-    for (int e = threadIdx.x; e < nk * LPT; e += blockDim.x) cp_async16(smem_u32(kst + e), Cp + e);
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
-    uint4* O = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * s * s + static_cast<size_t>(y) * s) * D);
+    uint4* O = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * s * s + static_cast<size_t>(lo)) * D);
+    const uint4* Cb = reinterpret_cast<const uint4*>(oc + static_cast<size_t>(bh) * keep_k * D);
+    // kept rows straight from o_compact: they do not wait for the source rows
     for (int e = threadIdx.x; e < s * LPT; e += blockDim.x) {
         const int x = e / LPT, part = e - x * LPT;
         const int t = slot[x];
-        if (t >= 0) {
-            O[e] = kst[t * LPT + part];
-        } else {
-            int x0, x1;
-            float lx;
-            axis_taps(x, ratio, sp, x0, x1, lx);
-            const float w00 = (1.f - ly) * (1.f - lx), w01 = (1.f - ly) * lx;
-            const float w10 = ly * (1.f - lx), w11 = ly * lx;
-            O[e] = blend4(stage[x0 * LPT + part], stage[x1 * LPT + part], stage[per_row + x0 * LPT + part],
-                          stage[per_row + x1 * LPT + part], w00, w01, w10, w11);
-        }
+        if (t >= 0) O[e] = __ldg(Cb + static_cast<size_t>(t) * LPT + part);
+    }
+    if (!mbar_wait(bar, 0, nullptr)) {
+        if (threadIdx.x == 0) atomicCAS(status, 0, VAR_ERR_TIMEOUT);
+        mbar_wait(bar, 0, nullptr);          // the copy must land before the CTA leaves
+        return;
+    }
+    const uint4* S1 = stage + (y1 != y0 ? per_row : 0);
+    for (int e = threadIdx.x; e < s * LPT; e += blockDim.x) {
+        const int x = e / LPT, part = e - x * LPT;
+        if (slot[x] >= 0) continue;
+        int x0, x1;
+        float lx;
+        axis_taps(x, ratio, sp, x0, x1, lx);
+        const float w00 = (1.f - ly) * (1.f - lx), w01 = (1.f - ly) * lx;
+        const float w10 = ly * (1.f - lx), w11 = ly * lx;
+        O[e] = blend4(stage[x0 * LPT + part], stage[x1 * LPT + part], S1[x0 * LPT + part], S1[x1 * LPT + part], w00,
+                      w01, w10, w11);
     }
 }
 
@@ -213,7 +232,7 @@ int launch_restore_d(int B, int H, int sp, int s, const __nv_bfloat16* P, const 
         return cuda_status(launch_kernel(fill_rows_kernel<D>, grid, dim3(256), 0, st, false, P, idx, keep_k, O, H,
                                          sp, s, ratio));
     }
-    const size_t smem = (2ull * sp + s) * LPT * sizeof(uint4) + sizeof(int) * s;
+    const size_t smem = 2ull * sp * LPT * sizeof(uint4) + sizeof(int) * s;
     if (smem > 200 * 1024) return VAR_ERR_UNSUPPORTED;
     if (ensure_smem_attr(restore_rows_kernel<D>, static_cast<int>(smem)) != cudaSuccess) return VAR_ERR_CUDA;
     return cuda_status(launch_kernel(restore_rows_kernel<D>, dim3(s, B * H), dim3(256), smem, st, false, P, C, idx,
