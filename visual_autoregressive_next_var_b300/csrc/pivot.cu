@@ -8,9 +8,9 @@
 //
 // The ranking is that of the fp64 evaluation (mean = fp64 channel sum / N,
 // score = fp64 pairwise-halving tree over channels of rounded squared
-// differences), reached with fp32 work on nearly every token.  Two kernels:
+// differences), reached with fp32 work on nearly every token.  Three kernels:
 //
-//   1. colsum (HBM pass over X).  Exact channel sums.  A cluster of 8 CTAs
+//   1. colsum (HBM pass over X).  Exact channel sums.  A cluster of 4 CTAs
 //      owns a 128-channel chunk of one batch element, each CTA a slab of
 //      rows streamed through a cp.async ring in shared memory.  Per element:
 //      x = hi + lo split exactly by two fp32 "magic" additions (hi a multiple
@@ -20,7 +20,8 @@
 //      The cluster merges its CTAs' partial sums through distributed shared
 //      memory; the exact sum is rounded once to fp64, divided by N (the fp64
 //      mean), and rounded to fp32 for the scores.
-//   2. score (L2 pass over X).  One warp per token: fp32 score with a
+//   2. score (L2 pass over X; the first chunks of each token are read before
+//      the wait for the means).  One warp per token: fp32 score with a
 //      rigorous bound eps_i >= |fp32 score - fp64 score| (below), stored as
 //      lo_i = score - eps (rounded down), hi_i = score + eps (rounded up).
 //   3. select, one 1024-thread CTA per batch element, keys in registers:
@@ -51,7 +52,7 @@ namespace varattn {
 
 namespace {
 
-constexpr int kSlabs = 8;                 // CTAs per cluster: row slabs of one chunk
+constexpr int kSlabs = 4;                 // CTAs per cluster: row slabs of one chunk
 constexpr int kChunk = 128;               // channels per chunk (256 bytes of a row)
 constexpr int kSegs = kChunk / 8;         // 16-byte segments of a chunk row
 constexpr int kSumThreads = 512;
@@ -349,20 +350,20 @@ __global__ void __cluster_dims__(kSlabs, 1, 1) __launch_bounds__(kSumThreads)
     }
     cluster_sync_all();
     // CTA `rank` finishes channels [rank*kPer, rank*kPer + kPer) of the chunk: thread
-    // (channel, peer) = (tid / 8, tid % 8) reads one peer's partial sums, the
-    // eight lanes of a channel add them
+    // (channel, peer) = (tid / kSlabs, tid % kSlabs) reads one peer's partial
+    // sums, the kSlabs lanes of a channel add them
     constexpr int kPer = kChunk / kSlabs;
     if (tid < kPer * kSlabs) {
-        const int cl = rank * kPer + (tid >> 3);
+        const int cl = rank * kPer + tid / kSlabs;
         const int cc = chunk * kChunk + cl;
         long long sp, sq;
-        ld_peer_pair(smem_u32(&part[cl][0]), static_cast<uint32_t>(tid & 7), sp, sq);
+        ld_peer_pair(smem_u32(&part[cl][0]), static_cast<uint32_t>(tid % kSlabs), sp, sq);
 #pragma unroll
         for (int off = 1; off < kSlabs; off <<= 1) {
             sp += __shfl_xor_sync(0xffffffffu, sp, off);
             sq += __shfl_xor_sync(0xffffffffu, sq, off);
         }
-        if ((tid & 7) == 0 && cc < C) {
+        if (tid % kSlabs == 0 && cc < C) {
             const __int128 t = static_cast<__int128>(sp) * (static_cast<__int128>(1) << 36) + static_cast<__int128>(sq);
             const double s = i128_to_f64_rn(t) * 0x1p-60;     // exact power-of-two scaling
             const double m = __ddiv_rn(s, static_cast<double>(N));
@@ -385,6 +386,28 @@ __global__ void __launch_bounds__(kScoreThreads, 4)
     const int b = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_launch_dependents();
+    const int nchunk = C / 8;                                           // 16-byte chunks per row
+    const int h1 = (nchunk + 31) / 32;
+    // the warp's tokens are scored together: one read of the means serves both
+    const int i0 = blockIdx.x * kScoreTok + warp * kTokPerWarp;
+    const uint4* rows[kTokPerWarp];
+    bool tv[kTokPerWarp];
+#pragma unroll
+    for (int t = 0; t < kTokPerWarp; ++t) {
+        tv[t] = i0 + t < N;
+        rows[t] = reinterpret_cast<const uint4*>(x + (static_cast<size_t>(b) * N + min(i0 + t, N - 1)) * C);
+    }
+    constexpr int kBatch = 4;                                           // chunks per token in flight
+    // X is not written by the colsum kernel: the first batch is read before
+    // waiting for the means
+    uint4 v[kTokPerWarp][kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+        const int ch = lane + 32 * k;
+#pragma unroll
+        for (int t = 0; t < kTokPerWarp; ++t)
+            v[t][k] = (ch < nchunk && tv[t]) ? __ldg(rows[t] + ch) : make_uint4(0u, 0u, 0u, 0u);
+    }
     pdl_wait();   // the channel means of the colsum kernel
 
     float ss = 0.f;
@@ -402,36 +425,25 @@ __global__ void __launch_bounds__(kScoreThreads, 4)
     for (int w = 0; w < kScoreWarps; ++w) n2 = __fadd_ru(n2, red[w]);
     const float mn = __fsqrt_ru(n2);                                    // >= ||m'||
     const float E = __fadd_ru(__fmul_ru(mn, 0x1.000002p-24f), 0x1p-120f);   // >= ||m' - mu||
-    const int nchunk = C / 8;                                           // 16-byte chunks per row
-    const int h1 = (nchunk + 31) / 32;
     const float c1 = static_cast<float>(h1 + 8 + 3) * 0x1p-24f;
     const float E3 = __fmul_ru(3.f, __fmul_ru(E, E));
     const float mn2 = __fadd_ru(__fmul_ru(mn, mn), 1.f);
     const uint64_t neg1 = f2_pack(-1.f, -1.f);
 
-    // the warp's tokens are scored together: one read of the means serves both
-    const int i0 = blockIdx.x * kScoreTok + warp * kTokPerWarp;
-    const uint4* rows[kTokPerWarp];
-    bool tv[kTokPerWarp];
-#pragma unroll
-    for (int t = 0; t < kTokPerWarp; ++t) {
-        tv[t] = i0 + t < N;
-        rows[t] = reinterpret_cast<const uint4*>(x + (static_cast<size_t>(b) * N + min(i0 + t, N - 1)) * C);
-    }
     uint64_t acc[kTokPerWarp][4];
 #pragma unroll
     for (int t = 0; t < kTokPerWarp; ++t)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[t][e] = 0ull;
-    constexpr int kBatch = 4;                                           // chunks per token in flight
     for (int k0 = 0; k0 < h1; k0 += kBatch) {
-        uint4 v[kTokPerWarp][kBatch];
+        if (k0 > 0) {
 #pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-            const int ch = lane + 32 * (k0 + k);
+            for (int k = 0; k < kBatch; ++k) {
+                const int ch = lane + 32 * (k0 + k);
 #pragma unroll
-            for (int t = 0; t < kTokPerWarp; ++t)
-                v[t][k] = (ch < nchunk && tv[t]) ? __ldg(rows[t] + ch) : make_uint4(0u, 0u, 0u, 0u);
+                for (int t = 0; t < kTokPerWarp; ++t)
+                    v[t][k] = (ch < nchunk && tv[t]) ? __ldg(rows[t] + ch) : make_uint4(0u, 0u, 0u, 0u);
+            }
         }
 #pragma unroll
         for (int k = 0; k < kBatch; ++k) {
