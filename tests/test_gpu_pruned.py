@@ -233,7 +233,10 @@ def test_pruned_keep_all_equals_dense():
 # ---------------------------------------------------------------- restore + scatter
 
 @pytest.mark.parametrize("sp,s,K,D", [(48, 64, 819, 128), (40, 48, 921, 128), (13, 16, 0, 64),
-                                      (13, 16, 256, 64), (5, 6, 7, 128), (64, 64, 100, 128)])
+                                      (13, 16, 256, 64), (5, 6, 7, 128), (64, 64, 100, 128),
+                                      (96, 128, 6554, 64),      # index list longer than 4096: row searches
+                                      (64, 80, 6400, 64),       # every token kept, searched rows full
+                                      (24, 32, 1024, 128)])     # every token kept, whole-list reads
 def test_restore_scatter(sp, s, K, D):
     B, H = 2, 3
     sides = (1, sp, s) if sp != s else (1, s, s)
