@@ -545,6 +545,12 @@ def extra_rows(V, dev, step: Step, inp, iters: int, peaks, host_bytes):
     t_sc = time_graph(lambda: V.var_sparvar_scores(p, d_sv, SINK_SIDE, tau_sv, q_src, step.k, sv_ws, sv_sc,
                                                    rescored=sv_rs), iters, flush)
     n_rescored = int(sv_rs.sum().item())
+    # the tensor-core scores from the decision step's row log2-sum-exp (the lse of
+    # its dense attention, computed above for the guided pivots)
+    sv_fast = torch.empty_like(sv_sc)
+    V.var_attn_dense_lse(p, src, q_src, step.k, step.v, o_src, lse)
+    t_fast = time_graph(lambda: V.var_sparvar_scores_fast(p, d_sv, SINK_SIDE, q_src, step.k, lse, sv_ws, sv_fast),
+                        iters, flush)
     t_sc_all = time_graph(lambda: V.var_sparvar_scores(p, d_sv, SINK_SIDE, tau_sv, q_src, step.k, sv_ws, sv_sc,
                                                        flags=V.VAR_SPARVAR_RESCORE_ALL), iters, flush)
     V.var_sparvar_scores(p, d_sv, SINK_SIDE, tau_sv, q_src, step.k, sv_ws, sv_sc)
@@ -560,14 +566,21 @@ def extra_rows(V, dev, step: Step, inp, iters: int, peaks, host_bytes):
                       iters, flush)
     pairs = mask_kept_pairs(WORKLOADS[W1024].sides, rp, en, sink, QBLOCK)
     fl_sv = 4.0 * B * H * pairs * D
+    A_fast = sv_fast.cpu().numpy()
+    rp_f, en_f, sink_f = V.var_sparvar_mask_build(p, d_sv, FINAL, SINK_SIDE, A_fast, tau_sv)
+    same_mask = bool(np.array_equal(rp_f, rp) and np.array_equal(en_f, en) and sink_f == sink)
     rows["sparvar_dynamic_mask_32_to_64"] = {
         "scores_ms": t_sc, "blocks_rescored_fp64": n_rescored, "blocks": nqb_sv,
+        "scores_fast_tensor_core_ms": t_fast, "fast_mask_equals_certified": same_mask,
+        "fast_max_rel_diff": float(np.max(np.abs(A_fast - A) / np.maximum(A, 1e-12))),
         "scores_all_blocks_fp64_ms": t_sc_all, "host_select_map_plan_ms": t_host, "attn_ms": t_sv,
         "density": pairs / (step.N[FINAL] * step.L[FINAL]), "TFLOP/s": fl_sv / t_sv / 1e9,
         "effective_dense_equiv_TFLOP/s": step.flops["attn_dense_1024px"] / t_sv / 1e9, "units": U_sv, "tau": tau_sv,
         "note": "decision step 32x32: block scores (certified fp32 on the CUDA cores, fp64 re-score of the "
                 "blocks the bound does not settle) -> host selection + index mapping -> block-sparse "
-                "attention of the 64x64 step",
+                "attention of the 64x64 step; scores_fast_tensor_core_ms: the same scores on the tensor cores "
+                "from the decision step's row log2-sum-exp (deterministic, no error bound); "
+                "fast_mask_equals_certified: the 64x64 mask built from them is the certified one",
         "timing": "CUDA graph replay after an L2 flush; host part timed once"}
     del q_src, o_src, o_sv
     # Branch Halving: the conditional half only, its rows repeated

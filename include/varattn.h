@@ -407,7 +407,8 @@ VAR_API int var_attn_blocksparse(const var_problem* p, int32_t step, const void*
 VAR_API int var_sparvar_units(const var_problem* p, int32_t decision_step, int32_t sink_max_side,
                               int32_t* n_units_out, int32_t* n_sink_units_out);
 
-/* Device workspace bytes var_sparvar_scores needs (0 for invalid arguments). */
+/* Device workspace bytes var_sparvar_scores and var_sparvar_scores_fast need
+ * (0 for invalid arguments). */
 VAR_API size_t var_sparvar_workspace_bytes(const var_problem* p, int32_t decision_step, int32_t sink_max_side);
 
 /* var_sparvar_scores flag: re-score every block in fp64, not only the unsettled ones. */
@@ -436,6 +437,26 @@ VAR_API size_t var_sparvar_workspace_bytes(const var_problem* p, int32_t decisio
 VAR_API int var_sparvar_scores(const var_problem* p, int32_t decision_step, int32_t sink_max_side, double tau,
                                int32_t flags, const void* q, const void* k, void* workspace,
                                size_t workspace_bytes, double* scores, int32_t* rescored, void* stream);
+
+/*
+ * Block scores of the decision step on the tensor cores, from the row
+ * log2-sum-exp its dense attention wrote (var_attn_dense_lse at
+ * decision_step): p_ij = 2^(q_i.k_j * scale * log2 e - lse_i), summed per
+ * (8x8 query block, unit) over the block's queries, the unit's keys, the heads
+ * and the batch, / (B H 64).  fp32 products and masses, fp64 sums in a fixed
+ * order: deterministic, but with no error bound -- the selection on these
+ * scores can differ from the fp64 definition's where candidates lie within
+ * the fp32 rounding of the cut (var_sparvar_scores decides those exactly).
+ * q, k as var_sparvar_scores; lse: device fp32 [B][H][N] (N = side^2 of the
+ * decision step).  scores: device fp64 [n_qb][U].  workspace:
+ * var_sparvar_workspace_bytes bytes, 256-byte aligned.  The decision side is
+ * at most 64 (64 query blocks).  Asynchronous on `stream`.
+ * Errors: as var_sparvar_scores (no tau or flags), VAR_ERR_UNSUPPORTED
+ * (decision side above 64, head_dim).
+ */
+VAR_API int var_sparvar_scores_fast(const var_problem* p, int32_t decision_step, int32_t sink_max_side,
+                                    const void* q, const void* k, const float* lse, void* workspace,
+                                    size_t workspace_bytes, double* scores, void* stream);
 
 /*
  * HOST: the target step's block mask from the decision step's scores (host

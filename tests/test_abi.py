@@ -235,6 +235,13 @@ def test_sparvar_rejects_bad_arguments():
     assert sc(C.byref(p), 9, 16, 0.5, 0, f, f, C.c_void_p(0x10010), ws, f, None, None) == V.VAR_ERR_UNSUPPORTED
     big = V.problem(2, 16, 128, (1, 2, 4, 8, 16, 32, 64, 96, 128, 160))     # 6 + 16 + 64 + 144 + 256 + 400 units
     assert sc(C.byref(big), 9, 16, 0.5, 0, f, f, f, 1 << 40, f, None, None) == V.VAR_ERR_UNSUPPORTED
+    fast = V.lib().var_sparvar_scores_fast
+    assert fast(C.byref(p), 9, 16, f, f, None, f, ws, f, None) == V.VAR_ERR_INVALID_ARG          # no lse
+    assert fast(C.byref(p), 9, 16, f, f, f, f, ws - 1, f, None) == V.VAR_ERR_WORKSPACE
+    assert fast(C.byref(p), 9, 16, f, f, C.c_void_p(0x10002), f, ws, f, None) == V.VAR_ERR_UNSUPPORTED
+    assert fast(C.byref(p), 7, 16, f, f, f, f, 1 << 40, f, None) == V.VAR_ERR_UNSUPPORTED       # side 20
+    wide = V.problem(2, 16, 128, (1, 2, 4, 8, 16, 32, 64, 72))                # 81 query blocks at side 72
+    assert fast(C.byref(wide), 7, 16, f, f, f, f, 1 << 40, f, None) == V.VAR_ERR_UNSUPPORTED
 
 
 def test_selftest_wait_timeout_rejects_bad_limits():

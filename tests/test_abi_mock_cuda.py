@@ -63,6 +63,7 @@ def _cases(V):
         ("var_attn_blocksparse", lambda: L.var_attn_blocksparse(C.byref(p), 9, f, f, f, C.byref(m), f, None)),
         ("var_attn_blocksparse_plan", lambda: L.var_attn_blocksparse(C.byref(p), 9, f, f, f, C.byref(mp), f, None)),
         ("var_sparvar_scores", lambda: L.var_sparvar_scores(C.byref(p), 9, 16, 0.8, 0, f, f, f, ws_sv, f, fs, None)),
+        ("var_sparvar_scores_fast", lambda: L.var_sparvar_scores_fast(C.byref(p), 9, 16, f, f, f, f, ws_sv, f, None)),
         ("var_selftest_wait_timeout", lambda: L.var_selftest_wait_timeout(1000, fs, None)),
         ("var_device_status", lambda: L.var_device_status(C.byref(out), 1)),
         ("var_check_status", lambda: L.var_check_status(fs, C.byref(out), 1, None)),

@@ -2,7 +2,10 @@
 scores (certified fp32, fp64 re-score of unsettled blocks), the host selection
 and index mapping, and block-sparse attention under the resulting mask --
 against the oracle's own pipeline: the mask the GPU path builds must equal,
-token for token, the mask the oracle builds from its own fp64 scores."""
+token for token, the mask the oracle builds from its own fp64 scores.  The
+tensor-core scores (no error bound) are checked against the oracle's values
+within the fp32 accuracy, for determinism, and for the same masks on these
+inputs."""
 import numpy as np
 import pytest
 import torch
@@ -185,4 +188,53 @@ def test_scores_many_units_head_dim_128():
         for ks in (9,):
             got_mask, _ = gpu_mask(p, sides, d, ks, sink, got, tau)
             assert np.array_equal(got_mask, oracle_mask(sides, d, ks, sink, A_ref, tau))
+    check_device_status()
+
+
+def gpu_scores_fast(p, d, sink, q, k):
+    """Tensor-core block scores from the decision step's row log2-sum-exp."""
+    B, H, N, D = q.shape
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=DEV)
+    o = torch.empty_like(q)
+    V.var_attn_dense_lse(p, d, q, k, k, o, lse)            # the values do not enter the row statistics
+    U, _ = V.var_sparvar_units(p, d, sink)
+    ws = torch.empty(V.var_sparvar_workspace_bytes(p, d, sink), dtype=torch.uint8, device=DEV)
+    sc = torch.full(((int(round(N ** 0.5)) // 8) ** 2, U), -1.0, dtype=torch.float64, device=DEV)
+    V.var_sparvar_scores_fast(p, d, sink, q, k, lse, ws, sc)
+    torch.cuda.synchronize()
+    return sc.cpu().numpy()
+
+
+@pytest.mark.parametrize("d,D", [(5, 128), (5, 64), (8, 64)])
+def test_fast_scores_close_to_oracle(d, D):
+    B, H, sink = 2, 2, 4
+    L, N = cache_len(SMALL, d), SMALL[d] ** 2
+    q = randn_bf16((B, H, N, D), 1201 + d)
+    k = randn_bf16((B, H, L + 64, D), 1202 + d)
+    p = V.problem(B, H, D, SMALL, kv_capacity=L + 64)
+    ref = oracle.sparvar_scores(q, k, SMALL, d, sink)
+    qd, kd = q.to(DEV), k.to(DEV)
+    got = gpu_scores_fast(p, d, sink, qd, kd)
+    assert np.all(np.isfinite(got))
+    assert np.allclose(got, ref, rtol=2e-3, atol=1e-7), np.max(np.abs(got - ref) / np.maximum(ref, 1e-7))
+    assert np.allclose(got.sum(axis=1), 1.0, rtol=0, atol=1e-3)
+    again = gpu_scores_fast(p, d, sink, qd, kd)
+    assert np.array_equal(got, again)                          # fixed summation order: deterministic
+    check_device_status()
+
+
+def test_fast_mask_1024px_decision_32_target_64():
+    w = WORKLOADS["pruned_1024px"]
+    d, ks, sink = 9, 12, 16
+    inp = make_inputs(w, steps=(d, ks))
+    B, H, D = w.batch, w.heads, w.head_dim
+    p = V.problem(B, H, D, w.sides, kv_capacity=inp.k.shape[2])
+    kd = inp.k.to(DEV)
+    A_ref = oracle.sparvar_scores(inp.q[d], inp.k, w.sides, d, sink)
+    A = gpu_scores_fast(p, d, sink, inp.q[d].to(DEV), kd)
+    assert np.allclose(A, A_ref, rtol=2e-3, atol=1e-7)
+    for tau in (0.5, 0.8, 0.95):
+        got_mask, _ = gpu_mask(p, w.sides, d, ks, sink, A, tau)
+        ref_mask = oracle_mask(w.sides, d, ks, sink, A_ref, tau)
+        assert np.array_equal(got_mask, ref_mask), f"tau {tau}: {np.sum(got_mask != ref_mask)} tokens differ"
     check_device_status()

@@ -90,6 +90,7 @@ _SIGS = {
     "var_sparvar_workspace_bytes": (C.c_size_t, [_PROB, C.c_int32, C.c_int32]),
     "var_sparvar_scores": (C.c_int, [_PROB, C.c_int32, C.c_int32, C.c_double, C.c_int32, _P, _P, _P, C.c_size_t,
                                      _P, _P, _P]),
+    "var_sparvar_scores_fast": (C.c_int, [_PROB, C.c_int32, C.c_int32, _P, _P, _P, _P, C.c_size_t, _P, _P]),
     "var_sparvar_mask_build": (C.c_int, [_PROB, C.c_int32, C.c_int32, C.c_int32, _P, C.c_double, _P, _P,
                                          C.c_int32, _P, _P, _P]),
     "var_selftest_wait_timeout": (C.c_int, [C.c_int32, _P, _P]),
@@ -305,6 +306,18 @@ def var_sparvar_scores(p: var_problem, decision_step: int, sink_max_side: int, t
            _lib.var_sparvar_scores(C.byref(p), decision_step, sink_max_side, tau, flags, _ptr(q), _ptr(k),
                                    _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(scores),
                                    _ptr(rescored), _stream(stream)))
+
+
+def var_sparvar_scores_fast(p: var_problem, decision_step: int, sink_max_side: int, q: torch.Tensor,
+                            k: torch.Tensor, lse: torch.Tensor, workspace: torch.Tensor, scores: torch.Tensor,
+                            stream=None) -> None:
+    """scores: device float64 [(side/8)^2, U] on the tensor cores from the decision step's
+    row log2-sum-exp lse (device float32 [B, H, side^2], as var_attn_dense_lse writes it);
+    deterministic fp32 masses with no error bound."""
+    _check("var_sparvar_scores_fast",
+           _lib.var_sparvar_scores_fast(C.byref(p), decision_step, sink_max_side, _ptr(q), _ptr(k), _ptr(lse),
+                                        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(scores),
+                                        _stream(stream)))
 
 
 def var_sparvar_mask_build(p: var_problem, decision_step: int, step: int, sink_max_side: int,

@@ -557,6 +557,26 @@ size_t var_sparvar_workspace_bytes(const var_problem* p, int32_t decision_step, 
     return varattn::sparvar_workspace_bytes(g, m.U);
 }
 
+int var_sparvar_scores_fast(const var_problem* p, int32_t decision_step, int32_t sink_max_side, const void* q,
+                            const void* k, const float* lse, void* workspace, size_t workspace_bytes, double* scores,
+                            void* stream)
+{
+    StepGeom g;
+    if (int rc = resolve(p, decision_step, &g)) return rc;
+    varattn::UnitMap m;
+    if (int rc = build_unit_map(p, decision_step, sink_max_side, &m)) return rc;
+    if (!q || !k || !lse || !workspace || !scores) return VAR_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || (reinterpret_cast<uintptr_t>(lse) & 3) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) || (reinterpret_cast<uintptr_t>(scores) & 7))
+        return VAR_ERR_UNSUPPORTED;
+    if (workspace_bytes < varattn::sparvar_workspace_bytes(g, m.U)) return VAR_ERR_WORKSPACE;
+    if ((g.side / 8) * (g.side / 8) > 64) return VAR_ERR_UNSUPPORTED;
+    int32_t* status = status_word(p);
+    if (!status) return VAR_ERR_CUDA;
+    return varattn::launch_sparvar_scores_fast(g, m, q, k, lse, workspace, workspace_bytes, scores,
+                                               static_cast<cudaStream_t>(stream), status);
+}
+
 int var_sparvar_scores(const var_problem* p, int32_t decision_step, int32_t sink_max_side, double tau, int32_t flags,
                        const void* q, const void* k, void* workspace, size_t workspace_bytes, double* scores,
                        int32_t* rescored, void* stream)

@@ -93,6 +93,10 @@ int launch_wait_timeout(int limit_us, cudaStream_t st, int32_t* status);
 int launch_sparvar_scores(const StepGeom& g, const UnitMap& m, const void* q, const void* k, double tau, int force,
                           double scale64, void* ws, size_t ws_bytes, double* scores, int32_t* rescored,
                           cudaStream_t st);
+// Block scores from the decision step's row log2-sum-exp on the tensor cores
+// (fp32, deterministic, no error bound).
+int launch_sparvar_scores_fast(const StepGeom& g, const UnitMap& m, const void* q, const void* k, const float* lse,
+                               void* ws, size_t ws_bytes, double* scores, cudaStream_t st, int32_t* status);
 int launch_restore_scatter(int B, int H, int D, int sp, int s, const void* prev, const void* oc,
                            const int32_t* idx, int keep_k, void* out, cudaStream_t st, int32_t* status,
                            bool fill_only);

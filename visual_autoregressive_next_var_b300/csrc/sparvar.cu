@@ -531,12 +531,320 @@ int launch_sparvar_d(const StepGeom& g, const UnitMap& m, const void* q, const v
     return VAR_OK;
 }
 
+
+// ------------------------------------------------------------------ fast path (tensor cores)
+
+// Block scores in fp32 from the decision step's row log2-sum-exp (written by
+// its dense attention): per (b, h) and 128 keys, S^T = K Q^T on the tensor
+// cores, p = 2^(s scale log2 e - lse_i), and the thread owning a key row adds
+// each group of 8 consecutive queries (one row of one 8x8 query block) into
+// that block's column of a shared-memory table.  A second kernel sums, per
+// (block, unit), the unit's keys over (b, h) in a fixed order (fp64), so the
+// result is deterministic.  No error bound: the selection on these scores can
+// differ from the fp64 definition's where two candidates are within the fp32
+// rounding of the cut.
+constexpr int kFastMaxQb = 64;       // query blocks of the decision step (side <= 64)
+
+template <int D>
+struct FastLayout {
+    static constexpr int HALVES = D / 64;
+    static constexpr int HALF_BYTES = 128 * 128;
+    static constexpr int TILE_BYTES = HALVES * HALF_BYTES;
+    static constexpr int NSQ = 2;
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_Q = OFF_K + TILE_BYTES;
+    static constexpr int OFF_LSE = OFF_Q + NSQ * TILE_BYTES;   // [4 warps][128] float
+    static constexpr int OFF_BAR = OFF_LSE + 4 * 128 * 4;
+    static constexpr int B_KF = 0;
+    static constexpr int B_QF = 1;                             // [NSQ]
+    static constexpr int B_QE = B_QF + NSQ;                    // [NSQ]
+    static constexpr int B_SF = B_QE + NSQ;                    // [2]
+    static constexpr int B_SE = B_SF + 2;                      // [2]
+    static constexpr int B_DR = B_SE + 2;
+    static constexpr int NBAR = B_DR + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int OFF_RED = OFF_MISC + 16;              // [n_qb][128] float
+    static constexpr uint32_t TMEM_COLS = 256;
+    static size_t smem_bytes(int n_qb) { return OFF_RED + static_cast<size_t>(n_qb) * 128 * 4 + 1024; }
+};
+
+struct FastMaps {
+    CUtensorMap q;    // 3-D (D, N', B*H), box (64, 128, 1)
+    CUtensorMap k;    // 3-D (D, L', B*H), box (64, 128, 1)
+};
+
+struct FastArgs {
+    int32_t n_q;            // N' (decision step queries)
+    int32_t side;           // its grid side (a multiple of 8)
+    int32_t n_qb;           // (side / 8)^2
+    int32_t n_qt;           // ceil(N' / 128)
+    int32_t L;              // keys of the decision step
+    int32_t n_kt;           // ceil(L / 128)
+    float scale_log2;
+    const float* lse;       // [B*H][N']
+    float* part;            // [B*H][n_qb][n_kt * 128]
+    int32_t* status;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256, 2) unit_mass_fast_kernel(const __grid_constant__ FastMaps maps, const FastArgs a)
+{
+    using Lay = FastLayout<D>;
+    constexpr int NSQ = Lay::NSQ;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t bar0 = sbase + Lay::OFF_BAR;
+    auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::OFF_MISC + 4);
+    float* red = reinterpret_cast<float*>(smem + Lay::OFF_RED);
+
+    const int bh = blockIdx.x / a.n_kt;
+    const int kt = blockIdx.x - bh * a.n_kt;
+    const int n_qt = a.n_qt;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(Lay::B_KF), 1);
+        for (int s = 0; s < NSQ; ++s) {
+            mbar_init(bar(Lay::B_QF + s), 1);
+            mbar_init(bar(Lay::B_QE + s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(Lay::B_SF + t), 1);
+            mbar_init(bar(Lay::B_SE + t), 128);
+        }
+        mbar_init(bar(Lay::B_DR), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&maps.q);
+        tma_prefetch_desc(&maps.k);
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(tmem_slot), Lay::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar(Lay::B_KF), Lay::TILE_BYTES);
+            for (int hh = 0; hh < Lay::HALVES; ++hh)
+                tma_load_3d(sbase + Lay::OFF_K + hh * Lay::HALF_BYTES, &maps.k, hh * 64, kt * 128, bh, bar(Lay::B_KF));
+            int issued = 0;
+            for (int t = 0; t < n_qt; ++t) {
+                const int s = t % NSQ;
+                if (!mbar_wait(bar(Lay::B_QE + s), ((t / NSQ) & 1) ^ 1, abort_flag)) {
+                    *abort_flag = 1;
+                    atomicCAS(a.status, 0, VAR_ERR_TIMEOUT);
+                    break;
+                }
+                mbar_arrive_expect_tx(bar(Lay::B_QF + s), Lay::TILE_BYTES);
+                for (int hh = 0; hh < Lay::HALVES; ++hh)
+                    tma_load_3d(sbase + Lay::OFF_Q + s * Lay::TILE_BYTES + hh * Lay::HALF_BYTES, &maps.q, hh * 64,
+                                t * 128, bh, bar(Lay::B_QF + s));
+                ++issued;
+            }
+            // every copy this thread started lands before the CTA may exit
+            mbar_wait(bar(Lay::B_KF), 0, nullptr);
+            for (int t = (issued > NSQ ? issued - NSQ : 0); t < issued; ++t)
+                mbar_wait(bar(Lay::B_QF + t % NSQ), (t / NSQ) & 1, nullptr);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ UMMA issuer: S^T = K Q^T
+        if (lane == 0) {
+            constexpr uint32_t IDESC = idesc_bf16(128, 128, false, false);
+            bool ok = mbar_wait(bar(Lay::B_KF), 0, abort_flag);
+            for (int t = 0; ok && t < n_qt; ++t) {
+                const int s = t % NSQ, buf = t & 1;
+                ok = mbar_wait(bar(Lay::B_QF + s), (t / NSQ) & 1, abort_flag) &&
+                     mbar_wait(bar(Lay::B_SE + buf), ((t >> 1) & 1) ^ 1, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t ka = sbase + Lay::OFF_K;
+                const uint32_t qa = sbase + Lay::OFF_Q + s * Lay::TILE_BYTES;
+                const uint32_t dst = tmem + static_cast<uint32_t>(buf * 128);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * Lay::HALF_BYTES + (kk % 4) * 32;
+                    umma_ss(dst, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024), IDESC,
+                            kk > 0 ? 1u : 0u);
+                }
+                umma_commit(bar(Lay::B_SF + buf));
+                umma_commit(bar(Lay::B_QE + s));
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                atomicCAS(a.status, 0, VAR_ERR_TIMEOUT);
+            }
+            umma_commit(bar(Lay::B_DR));
+            mbar_wait(bar(Lay::B_DR), 0, nullptr);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ consumers: one key row each
+        const int r = (warp & 3) * 32 + lane;
+        float* lw = reinterpret_cast<float*>(smem + Lay::OFF_LSE) + (warp & 3) * 128;
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const float sl2 = a.scale_log2;
+        const float* lse_bh = a.lse + static_cast<size_t>(bh) * a.n_q;
+        const int nb = a.side >> 3;
+        for (int qb = 0; qb < a.n_qb; ++qb) red[qb * 128 + r] = 0.f;
+        bool ok = true;
+        for (int t = 0; t < n_qt; ++t) {
+            const int buf = t & 1;
+            const int q0 = t * 128;
+            if (!mbar_wait(bar(Lay::B_SF + buf), (t >> 1) & 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            __syncwarp();                              // the previous tile's reads are done
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {              // columns past N': probability 0
+                const int qi = q0 + lane * 4 + e;
+                lw[lane * 4 + e] = qi < a.n_q ? __ldg(lse_bh + qi) : INFINITY;
+            }
+            __syncwarp();
+#pragma unroll
+            for (int c0 = 0; c0 < 128; c0 += 32) {
+                uint32_t sv[32];
+                tmem_ld32(tmem + lane_base + static_cast<uint32_t>(buf * 128 + c0), sv);
+                tmem_wait_ld();
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    // queries q0 + c0 + 8 g8 .. + 7: one row of one 8x8 query block
+                    float sum = 0.f;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const int col = 8 * g8 + c;
+                        sum += ex2_approx(fmaf(__uint_as_float(sv[col]), sl2, -lw[c0 + col]));
+                    }
+                    const int i0 = q0 + c0 + 8 * g8;
+                    if (i0 < a.n_q) {
+                        const int y = i0 / a.side, x = i0 - y * a.side;
+                        red[((y >> 3) * nb + (x >> 3)) * 128 + r] += sum;
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(Lay::B_SE + buf));
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            atomicCAS(a.status, 0, VAR_ERR_TIMEOUT);
+        } else {
+            const int j = kt * 128 + r;
+            const size_t lpad = static_cast<size_t>(a.n_kt) * 128;
+            if (j < a.L)
+                for (int qb = 0; qb < a.n_qb; ++qb)
+                    a.part[(static_cast<size_t>(bh) * a.n_qb + qb) * lpad + j] = red[qb * 128 + r];
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, Lay::TMEM_COLS);
+    }
+}
+
+// scores[qb][u] = sum over (b, h) in order, then the unit's keys, of the block's
+// masses, / (B H 64); one warp per (block, unit), fp64, fixed order
+__global__ void __launch_bounds__(32)
+    unit_mass_fast_reduce(const UnitMap m, const float* __restrict__ part, int BH, int n_qb, int n_kt,
+                          double* __restrict__ scores)
+{
+    const int u = blockIdx.x, qb = blockIdx.y, lane = threadIdx.x;
+    const int j0 = unit_key(m, u, lane), j1 = unit_key(m, u, lane + 32);
+    const size_t lpad = static_cast<size_t>(n_kt) * 128;
+    double acc = 0.0;
+    for (int bh = 0; bh < BH; ++bh) {
+        const float* pr = part + (static_cast<size_t>(bh) * n_qb + qb) * lpad;
+        const double v0 = j0 >= 0 ? static_cast<double>(__ldg(pr + j0)) : 0.0;
+        const double v1 = j1 >= 0 ? static_cast<double>(__ldg(pr + j1)) : 0.0;
+        acc = __dadd_rn(acc, __dadd_rn(v0, v1));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc = __dadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
+    if (lane == 0) scores[static_cast<size_t>(qb) * m.U + u] = acc / (static_cast<double>(BH) * 64.0);
+}
+
+template <int D>
+int launch_sparvar_fast_d(const StepGeom& g, const UnitMap& m, const void* q, const void* k, const float* lse,
+                          void* ws, double* scores, cudaStream_t st, int32_t* status)
+{
+    using Lay = FastLayout<D>;
+    const int BH = g.B * g.H;
+    const int nb = g.side / 8, n_qb = nb * nb;
+    const int n_kt = (g.L + 127) / 128;
+    FastMaps maps;
+    const uint32_t box[3] = {64, 128, 1};
+    const uint64_t BHu = static_cast<uint64_t>(BH);
+    {
+        const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(g.N), BHu};
+        const uint64_t strides[2] = {D * 2ull, static_cast<uint64_t>(g.N) * D * 2ull};
+        if (int rc = encode_tmap_bf16(&maps.q, q, 3, dims, strides, box)) return rc;
+    }
+    {
+        const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(g.L), BHu};
+        const uint64_t strides[2] = {D * 2ull, static_cast<uint64_t>(g.cap) * D * 2ull};
+        if (int rc = encode_tmap_bf16(&maps.k, k, 3, dims, strides, box)) return rc;
+    }
+    FastArgs a = {};
+    a.n_q = g.N;
+    a.side = g.side;
+    a.n_qb = n_qb;
+    a.n_qt = (g.N + 127) / 128;
+    a.L = g.L;
+    a.n_kt = n_kt;
+    a.scale_log2 = g.scale * 1.4426950408889634f;
+    a.lse = lse;
+    a.part = static_cast<float*>(ws);
+    a.status = status;
+    const size_t smem = Lay::smem_bytes(n_qb);
+    auto kern = unit_mass_fast_kernel<D>;
+    if (ensure_smem_attr(kern, static_cast<int>(smem)) != cudaSuccess) return VAR_ERR_CUDA;
+    if (launch_kernel(kern, dim3(static_cast<unsigned>(BH * n_kt)), dim3(256), smem, st, false, maps, a) !=
+        cudaSuccess)
+        return VAR_ERR_CUDA;
+    return cuda_status(launch_kernel(unit_mass_fast_reduce, dim3(m.U, n_qb), dim3(32), 0, st, false, m,
+                                     static_cast<const float*>(ws), BH, n_qb, n_kt, scores));
+}
+
+size_t fast_part_bytes(const StepGeom& g)
+{
+    const int nb = g.side / 8;
+    const size_t n_kt = static_cast<size_t>((g.L + 127) / 128);
+    return static_cast<size_t>(g.B) * g.H * nb * nb * n_kt * 128 * sizeof(float);
+}
+
 }  // namespace
 
 size_t sparvar_workspace_bytes(const StepGeom& g, int U)
 {
     const int nb = g.side / 8;
-    return sv_ws_layout(g.B * g.H, nb * nb, U).total;
+    const size_t certified = sv_ws_layout(g.B * g.H, nb * nb, U).total;
+    const size_t fast = fast_part_bytes(g);
+    return certified > fast ? certified : fast;
+}
+
+int launch_sparvar_scores_fast(const StepGeom& g, const UnitMap& m, const void* q, const void* k, const float* lse,
+                               void* ws, size_t ws_bytes, double* scores, cudaStream_t st, int32_t* status)
+{
+    if (ws_bytes < sparvar_workspace_bytes(g, m.U)) return VAR_ERR_WORKSPACE;
+    const int nb = g.side / 8;
+    if (nb * nb > kFastMaxQb) return VAR_ERR_UNSUPPORTED;
+    if (g.D == 128) return launch_sparvar_fast_d<128>(g, m, q, k, lse, ws, scores, st, status);
+    if (g.D == 64) return launch_sparvar_fast_d<64>(g, m, q, k, lse, ws, scores, st, status);
+    return VAR_ERR_UNSUPPORTED;
 }
 
 int launch_sparvar_scores(const StepGeom& g, const UnitMap& m, const void* q, const void* k, double tau, int force,
