@@ -1,5 +1,6 @@
 // Dense and pruned (gathered-query) cross-scale attention: host launchers of
 // the shared kernel in attn_kernel.cuh.
+#include <cstring>
 #include <map>
 #include <mutex>
 #include <queue>
@@ -93,6 +94,14 @@ static int launch_attn(const StepGeom& g, const void* q, const void* k, const vo
         const uint64_t strides[2] = {D * 2ull, static_cast<uint64_t>(g.cap) * D * 2ull};
         if (int rc = encode_tmap_bf16(&tk, k, 3, dims, strides, box)) return rc;
         if (int rc = encode_tmap_bf16(&tv, v, 3, dims, strides, box)) return rc;
+    }
+    std::memset(&maps.o, 0, sizeof maps.o);
+    if (MODE == MODE_DENSE) {
+        // the output rows, for the epilogue's tile stores (all B*H, so a repeated
+        // half lands inside the map)
+        const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(n_rows), BH};
+        const uint64_t strides[2] = {D * 2ull, static_cast<uint64_t>(n_rows) * D * 2ull};
+        if (int rc = encode_tmap_bf16(&maps.o, o, 3, dims, strides, box)) return rc;
     }
     AttnArgs a = {};
     a.n_rows = n_rows;

@@ -20,7 +20,11 @@
 // Tensor memory (512 columns): S0 | S1 | O0 | O1.  P_t (bf16) overwrites the
 // first columns of S_t and feeds the PV product straight from tensor memory.
 // The softmax is the online one in fp32 with exp2; the running maximum is
-// only moved (and O rescaled) when a new maximum exceeds it by 2^8.
+// only moved (and O rescaled) when a new maximum exceeds it by 2^8.  Dense and
+// block-sparse tiles leave through the idle K ring: each softmax thread writes
+// its normalised row into a swizzled staging tile and one thread per group
+// stores it with tensor-map stores (gathered rows, which may scatter, are
+// written by their threads).
 //
 // Block-sparse CTAs own a 2x2 square of 8x8 query blocks (tile t = block row
 // t of the square, two blocks side by side).  Before the pipeline starts, the
@@ -43,6 +47,7 @@ enum : int { MODE_DENSE = 0, MODE_GATHER = 1, MODE_SPARSE = 2 };
 
 struct DenseMaps {
     CUtensorMap q, k, v;   // 3-D (D, rows, B*H), box (64, 128, 1)
+    CUtensorMap o;         // dense: 3-D (D, n_rows, B*H), box (64, 128, 1); the epilogue's tile stores
 };
 
 struct SparseMaps {
@@ -50,6 +55,7 @@ struct SparseMaps {
     CUtensorMap k_sink, v_sink;        // 3-D (D, sink_len, B*H), box (64, 64, 1)
     CUtensorMap k_sc[VAR_MAX_SCALES];  // 4-D (D, s, s, B*H) per non-sink scale, box (64, 8, 8, 1)
     CUtensorMap v_sc[VAR_MAX_SCALES];
+    CUtensorMap o;                     // 4-D (D, s_q, s_q, B*H), box (64, 8, 8, 1): the epilogue's block stores
 };
 
 template <int D>
@@ -767,7 +773,7 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
         if (ok) ok = mbar_wait(bar(Lay::B_OF), 0, abort_flag);
         // split CTA: group 1 hands its row's (m, l) to group 0, which merges
         // O_0 and O_1 (both in its tensor-memory lanes) into the output
-        float2* comb = reinterpret_cast<float2*>(smem + Lay::OFF_K);   // the K ring is idle now
+        float2* comb = reinterpret_cast<float2*>(smem + Lay::OFF_V);   // the V ring is idle now
         float a0 = 1.f, a1 = 0.f;
         if (split) {
             if (g == 1) {
@@ -783,9 +789,8 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
                 m_run = mm;
             }
         }
-        if (!ok) {
-            record_fault(abort_flag, args.status, VAR_ERR_TIMEOUT);
-        } else if (!split || g == 0) {
+        if (!ok) record_fault(abort_flag, args.status, VAR_ERR_TIMEOUT);
+        if (!split || g == 0) {
             tc_fence_after();
             // destination row of this thread, or none
             __nv_bfloat16* dst = nullptr;
@@ -802,11 +807,14 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
             }
             const bool any = l_run > 0.f;            // a row that kept no key is written as zeros
             const float inv = any ? 1.0f / l_run : 0.f;
-            if (!SPARSE && !GATHER && args.lse && qrow < args.n_rows)
+            if (ok && !SPARSE && !GATHER && args.lse && qrow < args.n_rows)
                 args.lse[static_cast<size_t>(bh) * args.n_rows + qrow] = any ? m_run + log2f(l_run) : -INFINITY;
             const uint32_t tO1 = tmem + lane_base + Lay::COL_O1;
+            // dense and block-sparse: the normalised tile is staged in the idle K ring
+            // (128-byte swizzle, as the loads) and written by tensor-map stores
+            uint8_t* st_tile = smem + Lay::OFF_K + g * Lay::TILE_BYTES;
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int c0 = 0; c0 < D && ok; c0 += 32) {
                 uint32_t o[32];
                 tmem_ld32(tO + c0, o);
                 if (split) {
@@ -819,21 +827,51 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
                                                (a1 != 0.f ? __uint_as_float(o1[c]) * a1 : 0.f));
                 }
                 tmem_wait_ld();
-                if (dst) {
-                    uint32_t w[16];
+                uint32_t w[16];
 #pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        w[c] = any ? pack_bf16x2(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv)
-                                   : 0u;
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+                for (int c = 0; c < 16; ++c)
+                    w[c] = any ? pack_bf16x2(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv)
+                               : 0u;
+                if constexpr (GATHER) {
+                    if (dst) {
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) d4[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-                    if (args.o_repeat) {
-                        uint4* r4 = reinterpret_cast<uint4*>(dst + args.o_repeat + c0);
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            r4[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+                        for (int c = 0; c < 4; ++c) d4[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
                     }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int col = c0 + 8 * c;          // first of the 8 columns of this 16-byte chunk
+                        const int hh = col >> 6, cc = (col & 63) >> 3;
+                        *reinterpret_cast<uint4*>(st_tile + hh * Lay::HALF_BYTES + r * 128 + ((cc ^ (r & 7)) << 4)) =
+                            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+                    }
+                }
+            }
+            if constexpr (!GATHER) {
+                // every thread of the group arrives, whatever its status; the tile is
+                // stored only if all of it was written
+                fence_proxy_async_smem();
+                const bool all_ok = bar_red_and(2 + g, 128, ok);
+                if (all_ok && r == 0) {
+                    const uint32_t src = smem_u32(st_tile);
+                    if constexpr (SPARSE) {
+                        for (int hb = 0; hb < 2; ++hb) {
+                            const int by = by0 + g, bx = bx0 + hb;
+                            if (by >= args.nb || bx >= args.nb) continue;
+                            for (int hh = 0; hh < Lay::HALVES; ++hh)
+                                tma_store_4d(&maps.o, hh * 64, bx * 8, by * 8, bh,
+                                             src + hh * Lay::HALF_BYTES + hb * (Lay::HALF_BYTES / 2));
+                        }
+                    } else {
+                        const int bh_rep = args.o_repeat ? static_cast<int>(args.o_repeat / (static_cast<int64_t>(args.n_rows) * D)) : 0;
+                        for (int rep = 0; rep < (args.o_repeat ? 2 : 1); ++rep)
+                            for (int hh = 0; hh < Lay::HALVES; ++hh)
+                                tma_store_3d(&maps.o, hh * 64, row0 + g * 128, bh + rep * bh_rep,
+                                             src + hh * Lay::HALF_BYTES);
+                    }
+                    bulk_commit();
+                    bulk_wait_read0();
                 }
             }
         }

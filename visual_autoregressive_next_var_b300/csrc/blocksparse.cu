@@ -43,6 +43,14 @@ static int launch_sparse(const StepGeom& g, const int32_t* sides, int step, cons
         const uint32_t box[4] = {64, 8, 8, 1};
         if (int rc = encode_tmap_bf16(&maps.q, q, 4, dims, strides, box)) return rc;
     }
+    {
+        // the output grid, for the epilogue's 8x8 block stores
+        const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(g.side),
+                                  static_cast<uint64_t>(g.side), BH};
+        const uint64_t strides[3] = {row_bytes, g.side * row_bytes, static_cast<uint64_t>(g.N) * row_bytes};
+        const uint32_t box[4] = {64, 8, 8, 1};
+        if (int rc = encode_tmap_bf16(&maps.o, o, 4, dims, strides, box)) return rc;
+    }
     const int sink_extent = mask->sink_len > 0 ? mask->sink_len : 1;
     {
         const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(sink_extent), BH};

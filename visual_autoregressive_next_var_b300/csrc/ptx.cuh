@@ -87,6 +87,16 @@ __device__ __forceinline__ void named_bar_sync(int id, int n)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
+// Named barrier `id` over `n` threads that also ANDs a predicate across them.
+__device__ __forceinline__ bool bar_red_and(int id, int n, bool p)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+                 "bar.red.and.pred po, %2, %3, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+                 : "=r"(r) : "r"(static_cast<uint32_t>(p)), "r"(id), "r"(n) : "memory");
+    return r != 0;
+}
+
 __device__ __forceinline__ void named_bar_arrive(int id, int n)
 {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -113,6 +123,25 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int3
         "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
         : "memory");
 }
+
+// Shared -> global tile stores (bulk group completion); the source must stay
+// unchanged until bulk_wait_read0() returns.
+__device__ __forceinline__ void tma_store_3d(const void* tmap, int32_t c0, int32_t c1, int32_t c2, uint32_t src)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
+                 ::"l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(src) : "memory");
+}
+
+__device__ __forceinline__ void tma_store_4d(const void* tmap, int32_t c0, int32_t c1, int32_t c2, int32_t c3,
+                                             uint32_t src)
+{
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4}], [%5];"
+                 ::"l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(src) : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap)
 {
