@@ -3,16 +3,18 @@
 // Up is bilinear with half-pixel centres and edge clamp; the scatter overwrites
 // the kept rows.
 //
-// Scatter mode: restore_rows_kernel, one CTA per output grid row y and (b, h).
-// One thread issues two bulk copies (cp.async.bulk, completion on an mbarrier)
-// of the source rows y0, y1 of prev (2 x s' tokens, contiguous) into shared
-// memory.  Meanwhile the CTA finds the kept tokens of row y: index lists of up
-// to 4,096 entries are read whole (one coalesced pass, every entry in the row
-// marks its token), longer ones by two 32-ary searches for the row's slice.
-// The kept tokens are copied from o_compact straight away (they need no
-// source row); once the source rows have landed every other token is the
-// blend of four staged taps.  Every row of out is written once, with 16-byte
-// stores.
+// Scatter mode: restore_rows_kernel, one 256-thread CTA per output grid row y
+// and (b, h).  One thread issues two bulk copies (cp.async.bulk, completion on
+// an mbarrier) of the source rows y0, y1 of prev (2 x s' tokens, contiguous)
+// into shared memory.  Meanwhile the CTA finds the kept tokens of row y: index
+// lists of up to 4,096 entries are read whole (each thread keeps four loads in
+// flight, the first issued before the CTA fills its per-token tap tables; an
+// entry in row y marks its token and joins the row's kept list), longer ones by
+// two 32-ary searches for the row's slice.  Then the warps split: four copy the
+// kept tokens' rows of o_compact (they need no source row, two loads in flight
+// per thread) while the other four blend every other token from four staged
+// taps once the source rows have landed.  Every row of out is written once,
+// with 16-byte stores.
 //
 // Fill mode (the kept rows are written by the in-place pruned attention, maybe
 // concurrently, so they must not be touched): fill_rows_kernel, one CTA per 64
@@ -94,20 +96,32 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 
 constexpr int kScanMax = 4096;   // index lists up to this length are read whole by every CTA
 
+constexpr int kRowThreads = 256;
+constexpr int kKeptWarps = 4;    // warps that copy the kept tokens; the other four blend
+constexpr int kIdxBatch = 4;     // index entries each thread has in flight
+constexpr int kKeptBatch = 2;    // compact-row loads each kept-copy thread has in flight
+
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kRowThreads)
     restore_rows_kernel(const __nv_bfloat16* __restrict__ prev, const __nv_bfloat16* __restrict__ oc,
                         const int32_t* __restrict__ idx, int keep_k, __nv_bfloat16* __restrict__ out, int H, int sp,
                         int s, float ratio, int32_t* status)
 {
     constexpr int LPT = D / 8;
-    extern __shared__ __align__(128) uint4 stage[];       // [2][sp][LPT] source rows y0, y1, then [s] int
+    constexpr int KW = kKeptWarps, BT = kRowThreads - 32 * kKeptWarps;
+    // [2][sp][LPT] source rows y0, y1; then per token x of the row: the four
+    // tap weights, its two source columns (times LPT), an entry of the kept
+    // list (token, compact row) and its compact row or -1
+    extern __shared__ __align__(128) uint4 stage[];
     __shared__ __align__(8) uint64_t full;
-    __shared__ int range[2];
+    __shared__ int range[2], nkept;
     const int y = blockIdx.x, bh = blockIdx.y, b = bh / H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int per_row = sp * LPT;
-    int* slot = reinterpret_cast<int*>(stage + 2 * per_row);
+    float4* tw = reinterpret_cast<float4*>(stage + 2 * per_row);
+    int2* toff = reinterpret_cast<int2*>(tw + s);
+    int2* klist = toff + s;
+    int* slot = reinterpret_cast<int*>(klist + s);
     int y0, y1;
     float ly;
     axis_taps(y, ratio, sp, y0, y1, ly);
@@ -121,53 +135,100 @@ __global__ void __launch_bounds__(256)
         mbar_arrive_expect_tx(bar, (y1 != y0 ? 2u : 1u) * row_bytes);
         bulk_g2s(smem_u32(stage), P + static_cast<size_t>(y0) * per_row, row_bytes, bar);
         if (y1 != y0) bulk_g2s(smem_u32(stage + per_row), P + static_cast<size_t>(y1) * per_row, row_bytes, bar);
+        nkept = 0;
     }
-    for (int x = threadIdx.x; x < s; x += blockDim.x) slot[x] = -1;
     const int32_t* ib = idx + static_cast<size_t>(b) * keep_k;
     const int lo = y * s;
+    // the first entries of a whole-list read are in flight while the tables fill
+    int tk[kIdxBatch];
+#pragma unroll
+    for (int i = 0; i < kIdxBatch; ++i) {
+        const int j = i * kRowThreads + threadIdx.x;
+        tk[i] = (keep_k <= kScanMax && j < keep_k) ? __ldg(ib + j) - lo : -1;
+    }
+    for (int x = threadIdx.x; x < s; x += kRowThreads) {
+        slot[x] = -1;
+        int x0, x1;
+        float lx;
+        axis_taps(x, ratio, sp, x0, x1, lx);
+        tw[x] = make_float4((1.f - ly) * (1.f - lx), (1.f - ly) * lx, ly * (1.f - lx), ly * lx);
+        toff[x] = make_int2(x0 * LPT, x1 * LPT);
+    }
     if (keep_k > kScanMax && warp < 2) {
         const int r = warp_lower_bound(ib, keep_k, lo + warp * s);
         if (lane == 0) range[warp] = r;
     }
     __syncthreads();
+    // token t of the row is kept as compact row j (at most s entries are listed:
+    // more only for a list that is not strictly ascending)
+    auto mark = [&](int t, int j) {
+        slot[t] = j;
+        const int n = atomicAdd(&nkept, 1);
+        if (n < s) klist[n] = make_int2(t, j);
+    };
     if (keep_k <= kScanMax) {
-        for (int j = threadIdx.x; j < keep_k; j += blockDim.x) {
-            const int t = __ldg(ib + j) - lo;
-            if (t >= 0 && t < s) slot[t] = j;
+#pragma unroll
+        for (int i = 0; i < kIdxBatch; ++i)
+            if (tk[i] >= 0 && tk[i] < s) mark(tk[i], i * kRowThreads + threadIdx.x);
+        for (int j0 = kIdxBatch * kRowThreads; j0 < keep_k; j0 += kIdxBatch * kRowThreads) {
+#pragma unroll
+            for (int i = 0; i < kIdxBatch; ++i) {
+                const int j = j0 + i * kRowThreads + threadIdx.x;
+                tk[i] = j < keep_k ? __ldg(ib + j) - lo : -1;
+            }
+#pragma unroll
+            for (int i = 0; i < kIdxBatch; ++i)
+                if (tk[i] >= 0 && tk[i] < s) mark(tk[i], j0 + i * kRowThreads + threadIdx.x);
         }
     } else {
         const int j0 = range[0], nk = min(range[1] - range[0], s);
         if (threadIdx.x == 0 && range[1] - range[0] > s) atomicCAS(status, 0, VAR_ERR_INVALID_ARG);
-        for (int t = threadIdx.x; t < nk; t += blockDim.x) {
+        for (int t = threadIdx.x; t < nk; t += kRowThreads) {
             const int x = __ldg(ib + j0 + t) - lo;
-            if (x >= 0 && x < s) slot[x] = j0 + t;
+            if (x >= 0 && x < s) mark(x, j0 + t);
         }
     }
     __syncthreads();
     uint4* O = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * s * s + static_cast<size_t>(lo)) * D);
     const uint4* Cb = reinterpret_cast<const uint4*>(oc + static_cast<size_t>(bh) * keep_k * D);
-    // kept rows straight from o_compact: they do not wait for the source rows
-    for (int e = threadIdx.x; e < s * LPT; e += blockDim.x) {
-        const int x = e / LPT, part = e - x * LPT;
-        const int t = slot[x];
-        if (t >= 0) O[e] = __ldg(Cb + static_cast<size_t>(t) * LPT + part);
+    if (warp < KW) {
+        // kept tokens: copies of their compact rows, which need no source row
+        const int nk = min(nkept, s);
+        for (int k0 = threadIdx.x; k0 < nk * LPT; k0 += kKeptBatch * 32 * KW) {
+            uint4 v[kKeptBatch];
+            unsigned got = 0;
+#pragma unroll
+            for (int i = 0; i < kKeptBatch; ++i) {
+                const int k = k0 + i * 32 * KW;
+                if (k < nk * LPT) {
+                    const int item = k / LPT, part = k - item * LPT;
+                    v[i] = __ldg(Cb + static_cast<size_t>(klist[item].y) * LPT + part);
+                    got |= 1u << i;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kKeptBatch; ++i)
+                if (got >> i & 1u) {
+                    const int k = k0 + i * 32 * KW;
+                    const int item = k / LPT, part = k - item * LPT;
+                    O[klist[item].x * LPT + part] = v[i];
+                }
+        }
+        return;
     }
+    // every other token: the blend of four staged taps, once the source rows landed
     if (!mbar_wait(bar, 0, nullptr)) {
-        if (threadIdx.x == 0) atomicCAS(status, 0, VAR_ERR_TIMEOUT);
+        if (threadIdx.x == 32 * KW) atomicCAS(status, 0, VAR_ERR_TIMEOUT);
         mbar_wait(bar, 0, nullptr);          // the copy must land before the CTA leaves
         return;
     }
     const uint4* S1 = stage + (y1 != y0 ? per_row : 0);
-    for (int e = threadIdx.x; e < s * LPT; e += blockDim.x) {
+    for (int e = threadIdx.x - 32 * KW; e < s * LPT; e += BT) {
         const int x = e / LPT, part = e - x * LPT;
         if (slot[x] >= 0) continue;
-        int x0, x1;
-        float lx;
-        axis_taps(x, ratio, sp, x0, x1, lx);
-        const float w00 = (1.f - ly) * (1.f - lx), w01 = (1.f - ly) * lx;
-        const float w10 = ly * (1.f - lx), w11 = ly * lx;
-        O[e] = blend4(stage[x0 * LPT + part], stage[x1 * LPT + part], S1[x0 * LPT + part], S1[x1 * LPT + part], w00,
-                      w01, w10, w11);
+        const int2 o = toff[x];
+        const float4 w = tw[x];
+        O[e] = blend4(stage[o.x + part], stage[o.y + part], S1[o.x + part], S1[o.y + part], w.x, w.y, w.z, w.w);
     }
 }
 
@@ -232,10 +293,11 @@ int launch_restore_d(int B, int H, int sp, int s, const __nv_bfloat16* P, const 
         return cuda_status(launch_kernel(fill_rows_kernel<D>, grid, dim3(256), 0, st, false, P, idx, keep_k, O, H,
                                          sp, s, ratio));
     }
-    const size_t smem = 2ull * sp * LPT * sizeof(uint4) + sizeof(int) * s;
+    const size_t smem = 2ull * sp * LPT * sizeof(uint4) + (sizeof(float4) + 2 * sizeof(int2) + sizeof(int)) * s;
     if (smem > 200 * 1024) return VAR_ERR_UNSUPPORTED;
-    if (ensure_smem_attr(restore_rows_kernel<D>, static_cast<int>(smem)) != cudaSuccess) return VAR_ERR_CUDA;
-    return cuda_status(launch_kernel(restore_rows_kernel<D>, dim3(s, B * H), dim3(256), smem, st, false, P, C, idx,
+    // eight CTAs per SM (about 27 KB each at 48x48 -> 64x64) need the largest carveout
+    if (ensure_smem_attr(restore_rows_kernel<D>, static_cast<int>(smem), true) != cudaSuccess) return VAR_ERR_CUDA;
+    return cuda_status(launch_kernel(restore_rows_kernel<D>, dim3(s, B * H), dim3(kRowThreads), smem, st, false, P, C, idx,
                                      keep_k, O, H, sp, s, ratio, status));
 }
 

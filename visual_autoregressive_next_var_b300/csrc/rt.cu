@@ -133,18 +133,28 @@ cudaError_t current_device(int* dev)
     return (*dev < 0 || *dev >= 64) ? cudaErrorInvalidDevice : cudaSuccess;
 }
 
-cudaError_t ensure_smem_attr_raw(const void* func, int bytes)
+cudaError_t ensure_smem_attr_raw(const void* func, int bytes, bool max_carveout)
 {
     int dev = 0;
     if (cudaError_t e = current_device(&dev)) return e;
-    if (rt_mocked()) return rt().func_set_attribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (rt_mocked()) {
+        if (cudaError_t e = rt().func_set_attribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) return e;
+        return max_carveout ? rt().func_set_attribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, 100)
+                            : cudaSuccess;
+    }
     static std::mutex mu;
-    static std::map<std::pair<int, const void*>, int> done;
+    static std::map<std::pair<int, const void*>, std::pair<int, bool>> done;   // bytes set, carveout set
     std::lock_guard<std::mutex> lk(mu);
-    auto it = done.find({dev, func});
-    if (it != done.end() && it->second >= bytes) return cudaSuccess;
-    if (cudaError_t e = rt().func_set_attribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) return e;
-    done[{dev, func}] = bytes;
+    auto& d = done[{dev, func}];
+    if (d.first < bytes) {
+        if (cudaError_t e = rt().func_set_attribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) return e;
+        d.first = bytes;
+    }
+    if (max_carveout && !d.second) {
+        if (cudaError_t e = rt().func_set_attribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, 100))
+            return e;
+        d.second = true;
+    }
     return cudaSuccess;
 }
 

@@ -43,8 +43,10 @@ bool rt_mocked();
 // The current device (VAR_ERR_CUDA-style failure as a non-zero return).
 cudaError_t current_device(int* dev);
 
-// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per device and function.
-cudaError_t ensure_smem_attr_raw(const void* func, int bytes);
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per device and
+// function; max_carveout also asks for the largest shared-memory carveout (for
+// a kernel whose resident CTAs per SM fill it).
+cudaError_t ensure_smem_attr_raw(const void* func, int bytes, bool max_carveout = false);
 
 // Launch `kern` on `st` with `args` converted to the kernel's parameter types.
 // pdl: allow the launch to start as a programmatic dependent of the preceding
@@ -75,9 +77,9 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
 
 // Set the dynamic shared memory limit of `kern` once per device.
 template <typename... KArgs>
-cudaError_t ensure_smem_attr(void (*kern)(KArgs...), int bytes)
+cudaError_t ensure_smem_attr(void (*kern)(KArgs...), int bytes, bool max_carveout = false)
 {
-    return ensure_smem_attr_raw(reinterpret_cast<const void*>(kern), bytes);
+    return ensure_smem_attr_raw(reinterpret_cast<const void*>(kern), bytes, max_carveout);
 }
 
 }  // namespace varattn
