@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kRowThreads)
                         int s, float ratio, int32_t* status)
 {
     constexpr int LPT = D / 8;
-    constexpr int KW = kKeptWarps, BT = kRowThreads - 32 * kKeptWarps;
+    constexpr int KW = kKeptWarps;
     // [2][sp][LPT] source rows y0, y1; then per token x of the row: the four
     // tap weights, its two source columns (times LPT), an entry of the kept
     // list (token, compact row) and its compact row or -1
@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(kRowThreads)
         const int j = i * kRowThreads + threadIdx.x;
         tk[i] = (keep_k <= kScanMax && j < keep_k) ? __ldg(ib + j) - lo : -1;
     }
-    for (int x = threadIdx.x; x < s; x += kRowThreads) {
+    for (int x = threadIdx.x; x < s; x += blockDim.x) {
         slot[x] = -1;
         int x0, x1;
         float lx;
@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(kRowThreads)
     } else {
         const int j0 = range[0], nk = min(range[1] - range[0], s);
         if (threadIdx.x == 0 && range[1] - range[0] > s) atomicCAS(status, 0, VAR_ERR_INVALID_ARG);
-        for (int t = threadIdx.x; t < nk; t += kRowThreads) {
+        for (int t = threadIdx.x; t < nk; t += blockDim.x) {
             const int x = __ldg(ib + j0 + t) - lo;
             if (x >= 0 && x < s) mark(x, j0 + t);
         }
@@ -216,14 +216,15 @@ __global__ void __launch_bounds__(kRowThreads)
         }
         return;
     }
-    // every other token: the blend of four staged taps, once the source rows landed
+    // every other token: the blend of four staged taps, once the source rows
+    // landed (a run-time stride: unrolling this loop measured slower)
     if (!mbar_wait(bar, 0, nullptr)) {
         if (threadIdx.x == 32 * KW) atomicCAS(status, 0, VAR_ERR_TIMEOUT);
         mbar_wait(bar, 0, nullptr);          // the copy must land before the CTA leaves
         return;
     }
     const uint4* S1 = stage + (y1 != y0 ? per_row : 0);
-    for (int e = threadIdx.x - 32 * KW; e < s * LPT; e += BT) {
+    for (int e = threadIdx.x - 32 * KW; e < s * LPT; e += blockDim.x - 32 * KW) {
         const int x = e / LPT, part = e - x * LPT;
         if (slot[x] >= 0) continue;
         const int2 o = toff[x];
