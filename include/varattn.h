@@ -188,6 +188,10 @@ VAR_API int var_attn_pruned_scatter(const var_problem* p, int32_t step, const vo
  * Up(prev; s, s) to every row of out whose token is NOT in idx[b, :] and leaves
  * the rows in idx untouched (var_attn_pruned_scatter writes those).  The two
  * calls write disjoint rows, so they may run in either order or concurrently.
+ * Issued on the stream right after var_attn_pruned_scatter, its kernel starts
+ * beside that call's (a programmatic dependent launch: its blocks take the SMs
+ * the attention leaves free) and completes after it; after any other work it
+ * starts when that work has finished.
  * prev: [B][H][s'^2][D]; idx: [B][keep_k] strictly ascending, in [0, s^2);
  * out: [B][H][s^2][D].  step >= 1.
  * Errors: as var_restore_scatter.

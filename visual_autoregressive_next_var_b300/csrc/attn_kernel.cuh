@@ -326,6 +326,9 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::OFF_MISC + 4);
     const int2* U = reinterpret_cast<const int2*>(smem + Lay::OFF_U);
+    // in place (gathered rows scattered into the full grid): the fill of the
+    // other rows may start beside this grid; it reads and writes none of its rows
+    if (GATHER && args.scatter) pdl_launch_dependents();
 
     int bh, row0 = 0, by0 = 0, bx0 = 0;
     bool split = false;        // one query tile; group g takes key tiles j = g (mod 2)

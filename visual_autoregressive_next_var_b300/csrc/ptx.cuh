@@ -21,6 +21,19 @@ __device__ __forceinline__ uint32_t lane_id()
     return r;
 }
 
+// Programmatic dependent launch: let the next grid on the stream start (it
+// must not touch what this grid writes before it waits), and wait for the
+// preceding grid's completion and memory.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns()
 {
     uint64_t t;

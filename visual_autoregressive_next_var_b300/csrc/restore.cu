@@ -16,20 +16,18 @@
 // taps once the source rows have landed.  Every row of out is written once,
 // with 16-byte stores.
 //
-// Fill mode (the kept rows are written by the in-place pruned attention, maybe
-// concurrently, so they must not be touched): fill_rows_kernel, one CTA per 64
-// tokens of a (b, h); two warps find the chunk's slice of the ascending index
-// list with 32-ary searches (all lanes probing at once, one load round per
-// factor of 32 of the list's length), the slice is marked in shared memory,
-// and the other tokens are blended from prev.
+// Fill mode (var_restore_fill: the in-place pruned attention writes the kept
+// rows, maybe concurrently, so they must not be touched): the same kernel with
+// every warp blending and no kept copies.  It is launched as a programmatic
+// dependent: after the in-place attention, which lets it start at once, its
+// CTAs take the SMs the attention leaves free; one thread of CTA 0 waits for
+// the attention before its CTA exits, so the grid completes after it.
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace varattn {
 
 namespace {
-
-constexpr int kFillTok = 64;
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -105,10 +103,12 @@ template <int D>
 __global__ void __launch_bounds__(kRowThreads)
     restore_rows_kernel(const __nv_bfloat16* __restrict__ prev, const __nv_bfloat16* __restrict__ oc,
                         const int32_t* __restrict__ idx, int keep_k, __nv_bfloat16* __restrict__ out, int H, int sp,
-                        int s, float ratio, int32_t* status)
+                        int s, float ratio, int fill, int32_t* status)
 {
     constexpr int LPT = D / 8;
-    constexpr int KW = kKeptWarps;
+    // fill mode: the kept rows are not this kernel's (the in-place attention
+    // writes them), every warp blends
+    const int KW = fill ? 0 : kKeptWarps;
     // [2][sp][LPT] source rows y0, y1; then per token x of the row: the four
     // tap weights, its two source columns (times LPT), an entry of the kept
     // list (token, compact row) and its compact row or -1
@@ -163,6 +163,7 @@ __global__ void __launch_bounds__(kRowThreads)
     // more only for a list that is not strictly ascending)
     auto mark = [&](int t, int j) {
         slot[t] = j;
+        if (fill) return;
         const int n = atomicAdd(&nkept, 1);
         if (n < s) klist[n] = make_int2(t, j);
     };
@@ -231,54 +232,9 @@ __global__ void __launch_bounds__(kRowThreads)
         const float4 w = tw[x];
         O[e] = blend4(stage[o.x + part], stage[o.y + part], S1[o.x + part], S1[o.y + part], w.x, w.y, w.z, w.w);
     }
-}
-
-template <int D>
-__global__ void __launch_bounds__(256)
-    fill_rows_kernel(const __nv_bfloat16* __restrict__ prev, const int32_t* __restrict__ idx, int keep_k,
-                     __nv_bfloat16* __restrict__ out, int H, int sp, int s, float ratio)
-{
-    constexpr int LPT = D / 8;            // lanes per token row (16 B each)
-    constexpr int TPW = 32 / LPT;         // token rows per warp step
-    __shared__ uint8_t kept[kFillTok];
-    __shared__ int range[2];
-    const int N = s * s;
-    const int bh = blockIdx.y;
-    const int b = bh / H;
-    const int n0 = blockIdx.x * kFillTok;
-    const int n1 = min(N, n0 + kFillTok);
-    const int32_t* ib = idx + static_cast<size_t>(b) * keep_k;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    if (threadIdx.x < kFillTok) kept[threadIdx.x] = 0;
-    if (warp < 2) {
-        const int r = keep_k ? warp_lower_bound(ib, keep_k, warp ? n1 : n0) : 0;
-        if (lane == 0) range[warp] = r;
-    }
-    __syncthreads();
-    for (int j = range[0] + threadIdx.x; j < range[1]; j += blockDim.x) {
-        const int t = __ldg(ib + j) - n0;   // in [0, n1-n0) for an ascending list
-        if (t >= 0 && t < kFillTok) kept[t] = 1;
-    }
-    __syncthreads();
-
-    const int sub = lane / LPT, part = lane % LPT;
-    const uint4* P = reinterpret_cast<const uint4*>(prev + static_cast<size_t>(bh) * sp * sp * D);
-    uint4* O = reinterpret_cast<uint4*>(out + static_cast<size_t>(bh) * N * D);
-    for (int n = n0 + warp * TPW + sub; n < n1; n += 8 * TPW) {
-        if (kept[n - n0]) continue;
-        const int y = n / s, x = n - y * s;
-        int y0, y1, x0, x1;
-        float ly, lx;
-        axis_taps(y, ratio, sp, y0, y1, ly);
-        axis_taps(x, ratio, sp, x0, x1, lx);
-        const uint4 a = __ldg(P + static_cast<size_t>(y0 * sp + x0) * LPT + part);
-        const uint4 bq = __ldg(P + static_cast<size_t>(y0 * sp + x1) * LPT + part);
-        const uint4 c = __ldg(P + static_cast<size_t>(y1 * sp + x0) * LPT + part);
-        const uint4 d = __ldg(P + static_cast<size_t>(y1 * sp + x1) * LPT + part);
-        O[static_cast<size_t>(n) * LPT + part] = blend4(a, bq, c, d, (1.f - ly) * (1.f - lx), (1.f - ly) * lx,
-                                                        ly * (1.f - lx), ly * lx);
-    }
+    // a fill launched beside the in-place attention (programmatic dependent)
+    // completes only after it, so later work on the stream sees both
+    if (fill && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) pdl_wait();
 }
 
 template <int D>
@@ -287,19 +243,16 @@ int launch_restore_d(int B, int H, int sp, int s, const __nv_bfloat16* P, const 
                      bool fill_only)
 {
     constexpr int LPT = D / 8;
-    const int N = s * s;
     const float ratio = static_cast<float>(sp) / static_cast<float>(s);
-    if (fill_only) {
-        const dim3 grid((N + kFillTok - 1) / kFillTok, B * H);
-        return cuda_status(launch_kernel(fill_rows_kernel<D>, grid, dim3(256), 0, st, false, P, idx, keep_k, O, H,
-                                         sp, s, ratio));
-    }
     const size_t smem = 2ull * sp * LPT * sizeof(uint4) + (sizeof(float4) + 2 * sizeof(int2) + sizeof(int)) * s;
     if (smem > 200 * 1024) return VAR_ERR_UNSUPPORTED;
     // eight CTAs per SM (about 27 KB each at 48x48 -> 64x64) need the largest carveout
     if (ensure_smem_attr(restore_rows_kernel<D>, static_cast<int>(smem), true) != cudaSuccess) return VAR_ERR_CUDA;
-    return cuda_status(launch_kernel(restore_rows_kernel<D>, dim3(s, B * H), dim3(kRowThreads), smem, st, false, P, C, idx,
-                                     keep_k, O, H, sp, s, ratio, status));
+    // fill mode starts as a programmatic dependent of the preceding kernel (the
+    // in-place attention lets it start beside itself; any other kernel, when it finishes)
+    return cuda_status(launch_kernel(restore_rows_kernel<D>, dim3(s, B * H), dim3(kRowThreads), smem, st, fill_only,
+                                     P, fill_only ? nullptr : C, idx, keep_k, O, H, sp, s, ratio, fill_only ? 1 : 0,
+                                     status));
 }
 
 }  // namespace
