@@ -62,7 +62,7 @@ __device__ __forceinline__ uint4 blend4(const uint4& a, const uint4& b, const ui
     return r;
 }
 
-// ------------------------------------------------------------------ fill mode
+// ------------------------------------------------------------------ index search
 
 // First index of a[0, n) (ascending) whose value is >= key; every lane of the
 // warp calls it and gets the result.
@@ -84,7 +84,7 @@ __device__ __forceinline__ int warp_lower_bound(const int32_t* a, int n, int key
     return lo + __popc(__ballot_sync(0xffffffffu, below));
 }
 
-// ------------------------------------------------------------------ scatter mode
+// ------------------------------------------------------------------ row kernel
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
 {
