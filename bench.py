@@ -487,10 +487,9 @@ def extra_rows(V, dev, step: Step, inp, iters: int, peaks, host_bytes):
     p, s = step.p, FINAL
 
     def fused():
-        # disjoint rows: the fill starts beside the attention (programmatic
-        # dependent launch) on the SMs the attention leaves free
-        V.var_attn_pruned_scatter(p, s, step.q[s], step.k, step.v, step.idx[s], step.K[s], step.out[s])
-        V.var_restore_fill(p, s, step.out[MID], step.idx[s], step.K[s], step.out[s])
+        # one call: the fill starts beside the attention (programmatic dependent
+        # launch) on the SMs the attention leaves free; disjoint rows
+        V.var_pruned_in_place(p, s, step.q[s], step.k, step.v, step.out[MID], step.idx[s], step.K[s], step.out[s])
 
     t = time_graph(fused, iters, flush)
     t_attn = time_graph(lambda: V.var_attn_pruned_scatter(p, s, step.q[s], step.k, step.v, step.idx[s], step.K[s],
@@ -498,8 +497,8 @@ def extra_rows(V, dev, step: Step, inp, iters: int, peaks, host_bytes):
     t_chain = time_graph(lambda: (calls["attn_pruned_64"](), calls["restore_scatter_48to64"]()), iters, flush)
     rows["pruned_64_attn_and_restore_fused"] = {
         "ms": t, "attn_in_place_alone_ms": t_attn, "unfused_ms": t_chain,
-        "note": "in place: the attention writes its rows into the full grid and the fill, started beside it, "
-                "writes the rest; unfused: compact attention output, then restore + scatter",
+        "note": "var_pruned_in_place: the attention writes its rows into the full grid and the fill, started "
+                "beside it, writes the rest; unfused: compact attention output, then restore + scatter",
         "timing": "CUDA graph replay after an L2 flush"}
     # attention-guided pivots (ARVAR): the 32x32 step's row statistics and saliency
     src = FINAL - 3

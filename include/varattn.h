@@ -187,17 +187,30 @@ VAR_API int var_attn_pruned_scatter(const var_problem* p, int32_t step, const vo
  * The reconstruction's upsampled part alone ("ARVAR" Eq. (8)-(9)): writes
  * Up(prev; s, s) to every row of out whose token is NOT in idx[b, :] and leaves
  * the rows in idx untouched (var_attn_pruned_scatter writes those).  The two
- * calls write disjoint rows, so they may run in either order or concurrently.
- * Issued on the stream right after var_attn_pruned_scatter, its kernel starts
- * beside that call's (a programmatic dependent launch: its blocks take the SMs
- * the attention leaves free) and completes after it; after any other work it
- * starts when that work has finished.
+ * calls write disjoint rows, so they may run in either order or concurrently
+ * (var_pruned_in_place runs both with the fill started beside the attention).
  * prev: [B][H][s'^2][D]; idx: [B][keep_k] strictly ascending, in [0, s^2);
  * out: [B][H][s^2][D].  step >= 1.
  * Errors: as var_restore_scatter.
  */
 VAR_API int var_restore_fill(const var_problem* p, int32_t step, const void* prev, const int32_t* idx,
                              int32_t keep_k, void* out, void* stream);
+
+/*
+ * The whole in-place pruned step ("ARVAR" Key Design 3, Eq. (8)-(9)): the
+ * work of var_attn_pruned_scatter then var_restore_fill on `stream`, with the
+ * fill's kernel started beside the attention's (a programmatic dependent
+ * launch: its blocks take the SMs the attention leaves free; it reads and
+ * writes none of the attention's rows) and completing after it.  out equals
+ * var_attn_pruned followed by var_restore_scatter, with no compact buffer.
+ * q, k, v, idx, keep_k: as var_attn_pruned_scatter (idx strictly ascending);
+ * prev: as var_restore_fill; out: [B][H][N][D].  step >= 1; keep_k = 0
+ * writes the upsampled grid alone (q, k, v, idx may then be NULL).
+ * Errors: as var_attn_pruned_scatter and var_restore_fill.
+ */
+VAR_API int var_pruned_in_place(const var_problem* p, int32_t step, const void* q, const void* k,
+                                const void* v, const void* prev, const int32_t* idx, int32_t keep_k,
+                                void* out, void* stream);
 
 /*
  * var_attn_dense that also writes each query row's log2-sum-exp of its scaled

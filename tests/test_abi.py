@@ -84,6 +84,14 @@ def test_pruned_restore_pivot_reject_bad_arguments():
     assert L.var_restore_fill(C.byref(p), 0, f, f, 4, f, None) == V.VAR_ERR_INVALID_ARG
     assert L.var_restore_fill(C.byref(p), 12, f, None, 3, f, None) == V.VAR_ERR_INVALID_ARG
     assert L.var_restore_fill(C.byref(p), 12, f, f, -1, f, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_pruned_in_place(C.byref(p), 0, f, f, f, f, f, 4, f, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_pruned_in_place(C.byref(p), 12, f, f, f, f, None, 3, f, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_pruned_in_place(C.byref(p), 12, None, f, f, f, f, 3, f, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_pruned_in_place(C.byref(p), 12, f, f, f, None, f, 3, f, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_pruned_in_place(C.byref(p), 12, f, f, f, f, f, -1, f, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_pruned_in_place(C.byref(p), 12, f, f, f, f, f, 4097, f, None) == V.VAR_ERR_INVALID_ARG
+    assert L.var_pruned_in_place(C.byref(p), 12, f, f, f, C.c_void_p(0x10008), f, 3, f, None) == \
+        V.VAR_ERR_UNSUPPORTED
     odd = V.problem(3, 16, 128, SCHEDULE_1024)
     assert L.var_attn_dense_halved(C.byref(odd), 12, f, f, f, f, None) == V.VAR_ERR_INVALID_ARG
     assert L.var_attn_dense_halved(C.byref(p), 12, f, None, f, f, None) == V.VAR_ERR_INVALID_ARG

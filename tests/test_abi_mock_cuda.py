@@ -55,6 +55,9 @@ def _cases(V):
         ("var_attn_pruned_scatter", lambda: L.var_attn_pruned_scatter(C.byref(p), 9, f, f, f, f, 204, f, None)),
         ("var_restore_scatter", lambda: L.var_restore_scatter(C.byref(p), 9, f, f, f, 204, f, None)),
         ("var_restore_fill", lambda: L.var_restore_fill(C.byref(p), 9, f, f, 204, f, None)),
+        ("var_pruned_in_place", lambda: L.var_pruned_in_place(C.byref(p), 9, f, f, f, f, f, 204, f, None)),
+        ("var_pruned_in_place_fill_only", lambda: L.var_pruned_in_place(C.byref(p), 9, None, None, None, f, None,
+                                                                        0, f, None)),
         ("var_attn_saliency", lambda: L.var_attn_saliency(C.byref(p), 8, f, f, f, f, None)),
         ("var_guided_pivot_select", lambda: L.var_guided_pivot_select(C.byref(p), 9, 8, f, 204, f, None, f, ws_gd,
                                                                       None)),

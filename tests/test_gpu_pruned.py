@@ -111,10 +111,11 @@ def test_pivot_single_token_and_large_grid():
 
 # ---------------------------------------------------------------- fused pruned step
 
-@pytest.mark.parametrize("fill_first", [False, True])
-def test_fused_pruned_step_equals_chain(fill_first):
-    """var_attn_pruned_scatter + var_restore_fill write the same output as
-    var_attn_pruned + var_restore_scatter, bit for bit, in either order."""
+@pytest.mark.parametrize("order", ["attn_then_fill", "fill_then_attn", "one_call"])
+def test_fused_pruned_step_equals_chain(order):
+    """var_attn_pruned_scatter + var_restore_fill (in either order), and
+    var_pruned_in_place (the fill started beside the attention), write the same
+    output as var_attn_pruned + var_restore_scatter, bit for bit."""
     w = WORKLOADS["pruned_1024px"]
     inp = make_inputs(w, steps=(12,))
     step = 12
@@ -135,12 +136,14 @@ def test_fused_pruned_step_equals_chain(fill_first):
     V.var_attn_pruned(p, step, qd, kd, vd, idx, K, oc)
     V.var_restore_scatter(p, step, prev, oc, idx, K, chain)
     fused = torch.full((B, H, N, D), float("nan"), dtype=torch.bfloat16, device=DEV)
-    if fill_first:
+    if order == "fill_then_attn":
         V.var_restore_fill(p, step, prev, idx, K, fused)
         V.var_attn_pruned_scatter(p, step, qd, kd, vd, idx, K, fused)
+    elif order == "attn_then_fill":
+        V.var_attn_pruned_scatter(p, step, qd, kd, vd, idx, K, fused)
+        V.var_restore_fill(p, step, prev, idx, K, fused)
     else:
-        V.var_attn_pruned_scatter(p, step, qd, kd, vd, idx, K, fused)
-        V.var_restore_fill(p, step, prev, idx, K, fused)
+        V.var_pruned_in_place(p, step, qd, kd, vd, prev, idx, K, fused)
     torch.cuda.synchronize()
     assert torch.equal(fused, chain)
     # against the oracle's own step: its pivots (equal to the GPU's, bit for
@@ -174,8 +177,18 @@ def test_fused_pruned_step_head_dim_64_ragged():
     fused = torch.full((B, H, N, D), float("nan"), dtype=torch.bfloat16, device=DEV)
     V.var_attn_pruned_scatter(p, step, q, k, v, idx, K, fused)
     V.var_restore_fill(p, step, prev, idx, K, fused)
+    one = torch.full((B, H, N, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    V.var_pruned_in_place(p, step, q, k, v, prev, idx, K, one)
     torch.cuda.synchronize()
     assert torch.equal(fused, chain)
+    assert torch.equal(one, chain)
+    # keep_k = 0: the upsampled grid alone, equal to a restore with nothing kept
+    empty = torch.full((B, H, N, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    V.var_pruned_in_place(p, step, None, None, None, prev, None, 0, empty)
+    up = torch.empty_like(chain)
+    V.var_restore_scatter(p, step, prev, oc, idx, 0, up)
+    torch.cuda.synchronize()
+    assert torch.equal(empty, up)
     # every row against the oracle: kept rows are attention rows, the rest the upsample
     ic = idx_c.numpy()
     qrows = (np.arange(B * H)[:, None] * N + ic[np.arange(B * H) // H]).reshape(-1)

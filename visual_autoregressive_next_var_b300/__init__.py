@@ -71,6 +71,7 @@ _SIGS = {
     "var_restore_scatter": (C.c_int, [_PROB, C.c_int32, _P, _P, _P, C.c_int32, _P, _P]),
     "var_attn_pruned_scatter": (C.c_int, [_PROB, C.c_int32, _P, _P, _P, _P, C.c_int32, _P, _P]),
     "var_restore_fill": (C.c_int, [_PROB, C.c_int32, _P, _P, C.c_int32, _P, _P]),
+    "var_pruned_in_place": (C.c_int, [_PROB, C.c_int32, _P, _P, _P, _P, _P, C.c_int32, _P, _P]),
     "var_attn_dense_halved": (C.c_int, [_PROB, C.c_int32, _P, _P, _P, _P, _P]),
     "var_guided_pivot_exact_workspace_bytes": (C.c_size_t, [_PROB, C.c_int32, C.c_int32]),
     "var_guided_pivot_select_exact": (C.c_int, [_PROB, C.c_int32, C.c_int32, _P, _P, C.c_int32, _P, _P, _P,
@@ -224,6 +225,14 @@ def var_restore_fill(p: var_problem, step: int, prev: torch.Tensor, idx: Optiona
                      out: torch.Tensor, stream=None) -> None:
     _check("var_restore_fill",
            _lib.var_restore_fill(C.byref(p), step, _ptr(prev), _ptr(idx), keep_k, _ptr(out), _stream(stream)))
+
+
+def var_pruned_in_place(p: var_problem, step: int, q: Optional[torch.Tensor], k: Optional[torch.Tensor],
+                        v: Optional[torch.Tensor], prev: torch.Tensor, idx: Optional[torch.Tensor], keep_k: int,
+                        out: torch.Tensor, stream=None) -> None:
+    _check("var_pruned_in_place",
+           _lib.var_pruned_in_place(C.byref(p), step, _ptr(q), _ptr(k), _ptr(v), _ptr(prev), _ptr(idx), keep_k,
+                                    _ptr(out), _stream(stream)))
 
 
 def var_attn_dense_halved(p: var_problem, step: int, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,

@@ -230,6 +230,27 @@ int var_restore_fill(const var_problem* p, int32_t step, const void* prev, const
                                   static_cast<cudaStream_t>(stream), status, true);
 }
 
+int var_pruned_in_place(const var_problem* p, int32_t step, const void* q, const void* k, const void* v,
+                        const void* prev, const int32_t* idx, int32_t keep_k, void* out, void* stream)
+{
+    StepGeom g;
+    if (int rc = resolve(p, step, &g)) return rc;
+    if (step < 1) return VAR_ERR_INVALID_ARG;
+    if (keep_k < 0 || keep_k > g.N) return VAR_ERR_INVALID_ARG;
+    if (!prev || !out || (keep_k > 0 && (!q || !k || !v || !idx))) return VAR_ERR_INVALID_ARG;
+    if (!aligned16(prev) || !aligned16(out)) return VAR_ERR_UNSUPPORTED;
+    if (keep_k > 0 && (!aligned16(q) || !aligned16(k) || !aligned16(v))) return VAR_ERR_UNSUPPORTED;
+    int32_t* status = status_word(p);
+    if (!status) return VAR_ERR_CUDA;
+    const auto st = static_cast<cudaStream_t>(stream);
+    VAR_DEBUG_CHECK_INDICES(idx, g.B, keep_k, g.N, true, status, st);
+    if (keep_k > 0)
+        if (int rc = launch_attn_pruned(g, q, k, v, idx, keep_k, out, st, status, true)) return rc;
+    // the fill's predecessor on the stream is the attention just launched
+    return launch_restore_scatter(g.B, g.H, g.D, p->side[step - 1], g.side, prev, nullptr, idx, keep_k, out, st,
+                                  status, true, keep_k > 0);
+}
+
 int var_attn_dense_lse(const var_problem* p, int32_t step, const void* q, const void* k, const void* v, void* o,
                        float* lse, void* stream)
 {

@@ -97,9 +97,12 @@ int launch_sparvar_scores(const StepGeom& g, const UnitMap& m, const void* q, co
 // (fp32, deterministic, no error bound).
 int launch_sparvar_scores_fast(const StepGeom& g, const UnitMap& m, const void* q, const void* k, const float* lse,
                                void* ws, size_t ws_bytes, double* scores, cudaStream_t st, int32_t* status);
+// fill_only: the rows not in idx only (oc unused).  beside: launch as a
+// programmatic dependent of the preceding kernel, which must be the in-place
+// attention of the same step (it lets the fill start beside itself).
 int launch_restore_scatter(int B, int H, int D, int sp, int s, const void* prev, const void* oc,
                            const int32_t* idx, int keep_k, void* out, cudaStream_t st, int32_t* status,
-                           bool fill_only);
+                           bool fill_only, bool beside = false);
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? VAR_OK : VAR_ERR_CUDA; }
 

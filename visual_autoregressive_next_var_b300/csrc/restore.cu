@@ -16,12 +16,13 @@
 // taps once the source rows have landed.  Every row of out is written once,
 // with 16-byte stores.
 //
-// Fill mode (var_restore_fill: the in-place pruned attention writes the kept
-// rows, maybe concurrently, so they must not be touched): the same kernel with
-// every warp blending and no kept copies.  It is launched as a programmatic
-// dependent: after the in-place attention, which lets it start at once, its
-// CTAs take the SMs the attention leaves free; one thread of CTA 0 waits for
-// the attention before its CTA exits, so the grid completes after it.
+// Fill mode (var_restore_fill, var_pruned_in_place: the in-place pruned
+// attention writes the kept rows, maybe concurrently, so they must not be
+// touched): the same kernel with every warp blending and no kept copies.  In
+// var_pruned_in_place it is launched as a programmatic dependent of that
+// call's attention, which lets it start at once: its CTAs take the SMs the
+// attention leaves free, and one thread of CTA 0 waits for the attention
+// before its CTA exits, so the grid completes after it.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__(kRowThreads)
 template <int D>
 int launch_restore_d(int B, int H, int sp, int s, const __nv_bfloat16* P, const __nv_bfloat16* C,
                      const int32_t* idx, int keep_k, __nv_bfloat16* O, cudaStream_t st, int32_t* status,
-                     bool fill_only)
+                     bool fill_only, bool beside)
 {
     constexpr int LPT = D / 8;
     const float ratio = static_cast<float>(sp) / static_cast<float>(s);
@@ -248,25 +249,23 @@ int launch_restore_d(int B, int H, int sp, int s, const __nv_bfloat16* P, const 
     if (smem > 200 * 1024) return VAR_ERR_UNSUPPORTED;
     // eight CTAs per SM (about 27 KB each at 48x48 -> 64x64) need the largest carveout
     if (ensure_smem_attr(restore_rows_kernel<D>, static_cast<int>(smem), true) != cudaSuccess) return VAR_ERR_CUDA;
-    // fill mode starts as a programmatic dependent of the preceding kernel (the
-    // in-place attention lets it start beside itself; any other kernel, when it finishes)
-    return cuda_status(launch_kernel(restore_rows_kernel<D>, dim3(s, B * H), dim3(kRowThreads), smem, st, fill_only,
-                                     P, fill_only ? nullptr : C, idx, keep_k, O, H, sp, s, ratio, fill_only ? 1 : 0,
-                                     status));
+    return cuda_status(launch_kernel(restore_rows_kernel<D>, dim3(s, B * H), dim3(kRowThreads), smem, st,
+                                     fill_only && beside, P, fill_only ? nullptr : C, idx, keep_k, O, H, sp, s, ratio,
+                                     fill_only ? 1 : 0, status));
 }
 
 }  // namespace
 
 int launch_restore_scatter(int B, int H, int D, int sp, int s, const void* prev, const void* oc,
                            const int32_t* idx, int keep_k, void* out, cudaStream_t st, int32_t* status,
-                           bool fill_only)
+                           bool fill_only, bool beside)
 {
     if (B * H > 65535) return VAR_ERR_UNSUPPORTED;
     auto* P = static_cast<const __nv_bfloat16*>(prev);
     auto* C = static_cast<const __nv_bfloat16*>(oc);
     auto* O = static_cast<__nv_bfloat16*>(out);
-    if (D == 128) return launch_restore_d<128>(B, H, sp, s, P, C, idx, keep_k, O, st, status, fill_only);
-    if (D == 64) return launch_restore_d<64>(B, H, sp, s, P, C, idx, keep_k, O, st, status, fill_only);
+    if (D == 128) return launch_restore_d<128>(B, H, sp, s, P, C, idx, keep_k, O, st, status, fill_only, beside);
+    if (D == 64) return launch_restore_d<64>(B, H, sp, s, P, C, idx, keep_k, O, st, status, fill_only, beside);
     return VAR_ERR_UNSUPPORTED;
 }
 
