@@ -249,7 +249,9 @@ def test_pruned_keep_all_equals_dense():
                                       (13, 16, 256, 64), (5, 6, 7, 128), (64, 64, 100, 128),
                                       (96, 128, 6554, 64),      # index list longer than 4096: row searches
                                       (64, 80, 6400, 64),       # every token kept, searched rows full
-                                      (24, 32, 1024, 128)])     # every token kept, whole-list reads
+                                      (24, 32, 1024, 128),      # every token kept, whole-list reads
+                                      (1, 2, 1, 128),           # the first restore: one source token
+                                      (8, 5, 3, 128)])          # a coarser output grid (ratio 1.6)
 def test_restore_scatter(sp, s, K, D):
     B, H = 2, 3
     sides = (1, sp, s) if sp != s else (1, s, s)
