@@ -44,7 +44,15 @@ __device__ __forceinline__ void axis_taps(int d, float ratio, int n_in, int& i0,
     w1 = src - static_cast<float>(i0);
 }
 
-// bilinear blend of four 16-byte groups (8 bf16 each)
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// bilinear blend of four 16-byte groups (8 bf16 each), two elements per
+// packed f32x2 operation
 __device__ __forceinline__ uint4 blend4(const uint4& a, const uint4& b, const uint4& c, const uint4& d, float w00,
                                         float w01, float w10, float w11)
 {
@@ -52,12 +60,18 @@ __device__ __forceinline__ uint4 blend4(const uint4& a, const uint4& b, const ui
     const uint32_t* Bw = &b.x;
     const uint32_t* Cw = &c.x;
     const uint32_t* Dw = &d.x;
+    const uint64_t W00 = f2_pack(w00, w00), W01 = f2_pack(w01, w01), W10 = f2_pack(w10, w10),
+                   W11 = f2_pack(w11, w11);
     uint4 r;
     uint32_t* R = &r.x;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        const float lo = w00 * bf_lo(A[e]) + w01 * bf_lo(Bw[e]) + w10 * bf_lo(Cw[e]) + w11 * bf_lo(Dw[e]);
-        const float hi = w00 * bf_hi(A[e]) + w01 * bf_hi(Bw[e]) + w10 * bf_hi(Cw[e]) + w11 * bf_hi(Dw[e]);
+        uint64_t t = f2_mul(W00, f2_pack(bf_lo(A[e]), bf_hi(A[e])));
+        t = f2_fma(W01, f2_pack(bf_lo(Bw[e]), bf_hi(Bw[e])), t);
+        t = f2_fma(W10, f2_pack(bf_lo(Cw[e]), bf_hi(Cw[e])), t);
+        t = f2_fma(W11, f2_pack(bf_lo(Dw[e]), bf_hi(Dw[e])), t);
+        float lo, hi;
+        f2_unpack(t, lo, hi);
         R[e] = pack_bf16x2(lo, hi);
     }
     return r;
@@ -100,16 +114,16 @@ constexpr int kKeptWarps = 4;    // warps that copy the kept tokens; the other f
 constexpr int kIdxBatch = 4;     // index entries each thread has in flight
 constexpr int kKeptBatch = 2;    // compact-row loads each kept-copy thread has in flight
 
-template <int D>
+template <int D, bool FILL>
 __global__ void __launch_bounds__(kRowThreads)
     restore_rows_kernel(const __nv_bfloat16* __restrict__ prev, const __nv_bfloat16* __restrict__ oc,
                         const int32_t* __restrict__ idx, int keep_k, __nv_bfloat16* __restrict__ out, int H, int sp,
-                        int s, float ratio, int fill, int32_t* status)
+                        int s, float ratio, int32_t* status)
 {
     constexpr int LPT = D / 8;
     // fill mode: the kept rows are not this kernel's (the in-place attention
     // writes them), every warp blends
-    const int KW = fill ? 0 : kKeptWarps;
+    constexpr int KW = FILL ? 0 : kKeptWarps;
     // [2][sp][LPT] source rows y0, y1; then per token x of the row: the four
     // tap weights, its two source columns (times LPT), an entry of the kept
     // list (token, compact row) and its compact row or -1
@@ -164,7 +178,7 @@ __global__ void __launch_bounds__(kRowThreads)
     // more only for a list that is not strictly ascending)
     auto mark = [&](int t, int j) {
         slot[t] = j;
-        if (fill) return;
+        if (FILL) return;
         const int n = atomicAdd(&nkept, 1);
         if (n < s) klist[n] = make_int2(t, j);
     };
@@ -235,7 +249,7 @@ __global__ void __launch_bounds__(kRowThreads)
     }
     // a fill launched beside the in-place attention (programmatic dependent)
     // completes only after it, so later work on the stream sees both
-    if (fill && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) pdl_wait();
+    if (FILL && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) pdl_wait();
 }
 
 template <int D>
@@ -247,11 +261,11 @@ int launch_restore_d(int B, int H, int sp, int s, const __nv_bfloat16* P, const 
     const float ratio = static_cast<float>(sp) / static_cast<float>(s);
     const size_t smem = 2ull * sp * LPT * sizeof(uint4) + (sizeof(float4) + 2 * sizeof(int2) + sizeof(int)) * s;
     if (smem > 200 * 1024) return VAR_ERR_UNSUPPORTED;
+    auto kern = fill_only ? restore_rows_kernel<D, true> : restore_rows_kernel<D, false>;
     // eight CTAs per SM (about 27 KB each at 48x48 -> 64x64) need the largest carveout
-    if (ensure_smem_attr(restore_rows_kernel<D>, static_cast<int>(smem), true) != cudaSuccess) return VAR_ERR_CUDA;
-    return cuda_status(launch_kernel(restore_rows_kernel<D>, dim3(s, B * H), dim3(kRowThreads), smem, st,
-                                     fill_only && beside, P, fill_only ? nullptr : C, idx, keep_k, O, H, sp, s, ratio,
-                                     fill_only ? 1 : 0, status));
+    if (ensure_smem_attr(kern, static_cast<int>(smem), true) != cudaSuccess) return VAR_ERR_CUDA;
+    return cuda_status(launch_kernel(kern, dim3(s, B * H), dim3(kRowThreads), smem, st, fill_only && beside, P,
+                                     fill_only ? nullptr : C, idx, keep_k, O, H, sp, s, ratio, status));
 }
 
 }  // namespace
