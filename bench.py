@@ -495,6 +495,17 @@ def extra_rows(V, dev, step: Step, inp, iters: int, peaks, host_bytes):
     t_attn = time_graph(lambda: V.var_attn_pruned_scatter(p, s, step.q[s], step.k, step.v, step.idx[s], step.K[s],
                                                           step.out[s]), iters, flush)
     t_chain = time_graph(lambda: (calls["attn_pruned_64"](), calls["restore_scatter_48to64"]()), iters, flush)
+    # the whole pruned 64x64 step: pivots, pruned attention and restore
+    t_step = time_graph(lambda: V.var_pruned_step(p, s, step.x[s], step.K[s], step.q[s], step.k, step.v, step.out[MID],
+                                                  step.idx[s], step.out[s], step.ws[s]), iters, flush)
+    t_step_chain = time_graph(lambda: (calls["pivot_select_64"](), calls["attn_pruned_64"](),
+                                       calls["restore_scatter_48to64"]()), iters, flush)
+    rows["pruned_64_whole_step_one_call"] = {
+        "ms": t_step, "three_calls_ms": t_step_chain,
+        "note": "var_pruned_step: pivot selection, then the in-place pruned attention started beside the selection "
+                "kernel, then the fill beside the attention; three calls: var_pivot_select, var_attn_pruned, "
+                "var_restore_scatter",
+        "timing": "CUDA graph replay after an L2 flush"}
     rows["pruned_64_attn_and_restore_fused"] = {
         "ms": t, "attn_in_place_alone_ms": t_attn, "unfused_ms": t_chain,
         "note": "var_pruned_in_place: the attention writes its rows into the full grid and the fill, started "

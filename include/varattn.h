@@ -213,6 +213,24 @@ VAR_API int var_pruned_in_place(const var_problem* p, int32_t step, const void* 
                                 void* out, void* stream);
 
 /*
+ * The whole pruned step in one call ("FastVAR", abstract: pivotal tokens
+ * only; "ARVAR" Key Design 2 and Key Design 3, Eq. (8)-(9)): var_pivot_select
+ * of x (writing idx), then var_pruned_in_place with those indices, on
+ * `stream`.  The pruned attention is launched as a programmatic dependent of
+ * the selection kernel: its blocks set up and load keys and values beside the
+ * selection and read idx once the selection has completed; the fill starts
+ * beside the attention.  idx and out equal those of var_pivot_select followed
+ * by var_pruned_in_place (and so of the unfused chain).
+ * x, channels, keep_k, idx, workspace: as var_pivot_select (no scores);
+ * q, k, v, prev, out: as var_pruned_in_place.  keep_k = 0 writes the
+ * upsampled grid alone (idx, q, k, v, workspace unused; they may be NULL).
+ * Errors: as var_pivot_select and var_pruned_in_place.
+ */
+VAR_API int var_pruned_step(const var_problem* p, int32_t step, const void* x, int32_t channels,
+                            int32_t keep_k, const void* q, const void* k, const void* v, const void* prev,
+                            int32_t* idx, void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * var_attn_dense that also writes each query row's log2-sum-exp of its scaled
  * scores, lse[b,h,i] = log2(sum_j 2^(s_ij)), s_ij = Q[b,h,i,:] . K[b,h,j,:] *
  * scale * log2(e) over the L keys, so that the attention probabilities are

@@ -92,6 +92,18 @@ def test_pruned_restore_pivot_reject_bad_arguments():
     assert L.var_pruned_in_place(C.byref(p), 12, f, f, f, f, f, 4097, f, None) == V.VAR_ERR_INVALID_ARG
     assert L.var_pruned_in_place(C.byref(p), 12, f, f, f, C.c_void_p(0x10008), f, 3, f, None) == \
         V.VAR_ERR_UNSUPPORTED
+    step = L.var_pruned_step
+    assert step(C.byref(p), 0, f, 2048, 819, f, f, f, f, f, f, f, ws, None) == V.VAR_ERR_INVALID_ARG
+    assert step(C.byref(p), 12, None, 2048, 819, f, f, f, f, f, f, f, ws, None) == V.VAR_ERR_INVALID_ARG
+    assert step(C.byref(p), 12, f, 2040, 819, f, f, f, f, f, f, f, ws, None) == V.VAR_ERR_INVALID_ARG
+    assert step(C.byref(p), 12, f, 2048, 4097, f, f, f, f, f, f, f, ws, None) == V.VAR_ERR_INVALID_ARG
+    assert step(C.byref(p), 12, f, 2048, 819, f, f, f, f, None, f, f, ws, None) == V.VAR_ERR_INVALID_ARG
+    assert step(C.byref(p), 12, f, 2048, 819, None, f, f, f, f, f, f, ws, None) == V.VAR_ERR_INVALID_ARG
+    assert step(C.byref(p), 12, f, 2048, 819, f, f, f, None, f, f, f, ws, None) == V.VAR_ERR_INVALID_ARG
+    assert step(C.byref(p), 12, f, 2048, 819, f, f, f, f, f, f, None, 0, None) == V.VAR_ERR_WORKSPACE
+    assert step(C.byref(p), 12, f, 2048, 819, f, f, f, f, f, f, f, ws - 1, None) == V.VAR_ERR_WORKSPACE
+    assert step(C.byref(p), 12, f, 2048, 819, f, f, f, C.c_void_p(0x10008), f, f, f, ws, None) == \
+        V.VAR_ERR_UNSUPPORTED
     odd = V.problem(3, 16, 128, SCHEDULE_1024)
     assert L.var_attn_dense_halved(C.byref(odd), 12, f, f, f, f, None) == V.VAR_ERR_INVALID_ARG
     assert L.var_attn_dense_halved(C.byref(p), 12, f, None, f, f, None) == V.VAR_ERR_INVALID_ARG

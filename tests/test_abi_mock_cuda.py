@@ -58,6 +58,10 @@ def _cases(V):
         ("var_pruned_in_place", lambda: L.var_pruned_in_place(C.byref(p), 9, f, f, f, f, f, 204, f, None)),
         ("var_pruned_in_place_fill_only", lambda: L.var_pruned_in_place(C.byref(p), 9, None, None, None, f, None,
                                                                         0, f, None)),
+        ("var_pruned_step", lambda: L.var_pruned_step(C.byref(p), 9, f, 256, 204, f, f, f, f, f, f, f, ws_piv,
+                                                      None)),
+        ("var_pruned_step_fill_only", lambda: L.var_pruned_step(C.byref(p), 9, f, 256, 0, None, None, None, f,
+                                                                None, f, None, 0, None)),
         ("var_attn_saliency", lambda: L.var_attn_saliency(C.byref(p), 8, f, f, f, f, None)),
         ("var_guided_pivot_select", lambda: L.var_guided_pivot_select(C.byref(p), 9, 8, f, 204, f, None, f, ws_gd,
                                                                       None)),

@@ -111,11 +111,12 @@ def test_pivot_single_token_and_large_grid():
 
 # ---------------------------------------------------------------- fused pruned step
 
-@pytest.mark.parametrize("order", ["attn_then_fill", "fill_then_attn", "one_call"])
+@pytest.mark.parametrize("order", ["attn_then_fill", "fill_then_attn", "one_call", "whole_step"])
 def test_fused_pruned_step_equals_chain(order):
-    """var_attn_pruned_scatter + var_restore_fill (in either order), and
-    var_pruned_in_place (the fill started beside the attention), write the same
-    output as var_attn_pruned + var_restore_scatter, bit for bit."""
+    """var_attn_pruned_scatter + var_restore_fill (in either order),
+    var_pruned_in_place (the fill started beside the attention) and
+    var_pruned_step (pivots, attention and fill chained in one call) write the
+    same output as var_attn_pruned + var_restore_scatter, bit for bit."""
     w = WORKLOADS["pruned_1024px"]
     inp = make_inputs(w, steps=(12,))
     step = 12
@@ -142,8 +143,13 @@ def test_fused_pruned_step_equals_chain(order):
     elif order == "attn_then_fill":
         V.var_attn_pruned_scatter(p, step, qd, kd, vd, idx, K, fused)
         V.var_restore_fill(p, step, prev, idx, K, fused)
-    else:
+    elif order == "one_call":
         V.var_pruned_in_place(p, step, qd, kd, vd, prev, idx, K, fused)
+    else:
+        idx2 = torch.full_like(idx, -1)
+        V.var_pruned_step(p, step, x, K, qd, kd, vd, prev, idx2, fused, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(idx2, idx)
     torch.cuda.synchronize()
     assert torch.equal(fused, chain)
     # against the oracle's own step: its pivots (equal to the GPU's, bit for
@@ -240,6 +246,43 @@ def test_pruned_keep_all_equals_dense():
     V.var_attn_dense(p, step, q.to(DEV), k.to(DEV), v.to(DEV), od)
     torch.cuda.synchronize()
     assert torch.equal(oc, od)
+    check_device_status()
+
+
+def test_pruned_step_one_call_head_dim_64_ragged():
+    """var_pruned_step at head_dim 64 on a 23x23 grid: its indices equal the
+    oracle's pivots bit for bit and its output equals var_pivot_select +
+    var_attn_pruned + var_restore_scatter bit for bit."""
+    sides, D, B, H, C_ = (1, 2, 4, 6, 9, 14, 20, 23), 64, 2, 3, 96
+    step = len(sides) - 1
+    L, N = cache_len(sides, step), sides[step] ** 2
+    qc, kc, vc = randn_bf16((B, H, N, D), 191), randn_bf16((B, H, L, D), 192), randn_bf16((B, H, L, D), 193)
+    prev_c = randn_bf16((B, H, 20 * 20, D), 194)
+    x_c = randn_bf16((B, N, C_), 195)
+    q, k, v, prev, x = qc.to(DEV), kc.to(DEV), vc.to(DEV), prev_c.to(DEV), x_c.to(DEV)
+    K = V.var_keep_count(N, 1, 5)
+    p = V.problem(B, H, D, sides)
+    ws = torch.empty(V.var_pivot_workspace_bytes(p, step, C_), dtype=torch.uint8, device=DEV)
+    idx = torch.empty((B, K), dtype=torch.int32, device=DEV)
+    V.var_pivot_select(p, step, x, K, idx, ws)
+    oc = torch.empty((B, H, K, D), dtype=torch.bfloat16, device=DEV)
+    chain = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=DEV)
+    V.var_attn_pruned(p, step, q, k, v, idx, K, oc)
+    V.var_restore_scatter(p, step, prev, oc, idx, K, chain)
+    one = torch.full((B, H, N, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    idx1 = torch.full_like(idx, -1)
+    V.var_pruned_step(p, step, x, K, q, k, v, prev, idx1, one, ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx1.cpu().numpy(), oracle.pivot_select(x_c, K)[0])
+    assert torch.equal(idx1, idx)
+    assert torch.equal(one, chain)
+    # nothing kept: the upsampled grid alone
+    up = torch.full((B, H, N, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    V.var_pruned_step(p, step, x, 0, None, None, None, prev, None, up, None)
+    ref = torch.empty_like(chain)
+    V.var_restore_scatter(p, step, prev, None, None, 0, ref)
+    torch.cuda.synchronize()
+    assert torch.equal(up, ref)
     check_device_status()
 
 

@@ -72,6 +72,8 @@ _SIGS = {
     "var_attn_pruned_scatter": (C.c_int, [_PROB, C.c_int32, _P, _P, _P, _P, C.c_int32, _P, _P]),
     "var_restore_fill": (C.c_int, [_PROB, C.c_int32, _P, _P, C.c_int32, _P, _P]),
     "var_pruned_in_place": (C.c_int, [_PROB, C.c_int32, _P, _P, _P, _P, _P, C.c_int32, _P, _P]),
+    "var_pruned_step": (C.c_int, [_PROB, C.c_int32, _P, C.c_int32, C.c_int32, _P, _P, _P, _P, _P, _P, _P,
+                                  C.c_size_t, _P]),
     "var_attn_dense_halved": (C.c_int, [_PROB, C.c_int32, _P, _P, _P, _P, _P]),
     "var_guided_pivot_exact_workspace_bytes": (C.c_size_t, [_PROB, C.c_int32, C.c_int32]),
     "var_guided_pivot_select_exact": (C.c_int, [_PROB, C.c_int32, C.c_int32, _P, _P, C.c_int32, _P, _P, _P,
@@ -233,6 +235,16 @@ def var_pruned_in_place(p: var_problem, step: int, q: Optional[torch.Tensor], k:
     _check("var_pruned_in_place",
            _lib.var_pruned_in_place(C.byref(p), step, _ptr(q), _ptr(k), _ptr(v), _ptr(prev), _ptr(idx), keep_k,
                                     _ptr(out), _stream(stream)))
+
+
+def var_pruned_step(p: var_problem, step: int, x: torch.Tensor, keep_k: int, q: Optional[torch.Tensor],
+                    k: Optional[torch.Tensor], v: Optional[torch.Tensor], prev: torch.Tensor,
+                    idx: Optional[torch.Tensor], out: torch.Tensor, workspace: Optional[torch.Tensor],
+                    stream=None) -> None:
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("var_pruned_step",
+           _lib.var_pruned_step(C.byref(p), step, _ptr(x), x.shape[-1], keep_k, _ptr(q), _ptr(k), _ptr(v),
+                                _ptr(prev), _ptr(idx), _ptr(out), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def var_attn_dense_halved(p: var_problem, step: int, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,

@@ -251,6 +251,35 @@ int var_pruned_in_place(const var_problem* p, int32_t step, const void* q, const
                                   status, true, keep_k > 0);
 }
 
+int var_pruned_step(const var_problem* p, int32_t step, const void* x, int32_t channels, int32_t keep_k,
+                    const void* q, const void* k, const void* v, const void* prev, int32_t* idx, void* out,
+                    void* workspace, size_t workspace_bytes, void* stream)
+{
+    StepGeom g;
+    if (int rc = check_pivot_args(p, step, x, channels, keep_k, idx, &g)) return rc;
+    if (step < 1) return VAR_ERR_INVALID_ARG;
+    if (!prev || !out || (keep_k > 0 && (!q || !k || !v))) return VAR_ERR_INVALID_ARG;
+    if (!aligned16(prev) || !aligned16(out)) return VAR_ERR_UNSUPPORTED;
+    if (keep_k > 0 && (!aligned16(q) || !aligned16(k) || !aligned16(v))) return VAR_ERR_UNSUPPORTED;
+    const size_t need = pivot_workspace_bytes(g.B, g.N, channels);
+    if (keep_k > 0 && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return VAR_ERR_WORKSPACE;
+    int32_t* status = status_word(p);
+    if (!status) return VAR_ERR_CUDA;
+    const auto st = static_cast<cudaStream_t>(stream);
+    const int sp = p->side[step - 1];
+    if (keep_k == 0)   // nothing kept: the upsampled grid alone
+        return launch_restore_scatter(g.B, g.H, g.D, sp, g.side, prev, nullptr, nullptr, 0, out, st, status, true);
+    // pivots, then the pruned attention as a programmatic dependent of the
+    // selection (it sets up beside it and reads the indices once they are
+    // written), then the fill as a dependent of the attention
+    if (int rc = launch_pivot_select(g.B, g.N, channels, x, keep_k, idx, nullptr, workspace, workspace_bytes, st,
+                                     status))
+        return rc;
+    if (int rc = launch_attn_pruned(g, q, k, v, idx, keep_k, out, st, status, true, true)) return rc;
+    return launch_restore_scatter(g.B, g.H, g.D, sp, g.side, prev, nullptr, idx, keep_k, out, st, status, true, true);
+}
+
 int var_attn_dense_lse(const var_problem* p, int32_t step, const void* q, const void* k, const void* v, void* o,
                        float* lse, void* stream)
 {

@@ -69,7 +69,7 @@ static TilePlan plan_tiles(int bh, int tiles_per_bh, int n_sms)
 template <int D, int MODE>
 static int launch_attn(const StepGeom& g, const void* q, const void* k, const void* v,
                        const int32_t* idx, int n_rows, void* o, cudaStream_t st, int32_t* status,
-                       bool halved = false, bool scatter = false, float* lse = nullptr)
+                       bool halved = false, bool scatter = false, float* lse = nullptr, bool pdl = false)
 {
     using Lay = AttnLayout<D>;
     auto kern = attn_kernel<D, MODE, DenseMaps>;
@@ -125,7 +125,7 @@ static int launch_attn(const StepGeom& g, const void* q, const void* k, const vo
     a.lse = lse;
     a.status = status;
     return cuda_status(launch_kernel(kern, dim3(static_cast<unsigned>(plan.grid)), dim3(384), Lay::SMEM_BYTES, st,
-                                     false, maps, a));
+                                     pdl, maps, a));
 }
 
 int launch_attn_dense(const StepGeom& g, const void* q, const void* k, const void* v, void* o,
@@ -137,10 +137,15 @@ int launch_attn_dense(const StepGeom& g, const void* q, const void* k, const voi
 }
 
 int launch_attn_pruned(const StepGeom& g, const void* q, const void* k, const void* v,
-                       const int32_t* idx, int keep_k, void* o, cudaStream_t st, int32_t* status, bool scatter)
+                       const int32_t* idx, int keep_k, void* o, cudaStream_t st, int32_t* status, bool scatter,
+                       bool after_select)
 {
-    if (g.D == 128) return launch_attn<128, MODE_GATHER>(g, q, k, v, idx, keep_k, o, st, status, false, scatter);
-    if (g.D == 64) return launch_attn<64, MODE_GATHER>(g, q, k, v, idx, keep_k, o, st, status, false, scatter);
+    if (g.D == 128)
+        return launch_attn<128, MODE_GATHER>(g, q, k, v, idx, keep_k, o, st, status, false, scatter, nullptr,
+                                             after_select);
+    if (g.D == 64)
+        return launch_attn<64, MODE_GATHER>(g, q, k, v, idx, keep_k, o, st, status, false, scatter, nullptr,
+                                            after_select);
     return VAR_ERR_UNSUPPORTED;
 }
 

@@ -609,6 +609,10 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax groups
+        // gathered rows: launched as a programmatic dependent of the pivot
+        // selection (var_pruned_step), the index list is read only once that
+        // grid has completed; a no-op for an ordinary launch
+        if constexpr (GATHER) pdl_wait();
         const int g = (warp - 4) >> 2;
         const int r = (warp & 3) * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;

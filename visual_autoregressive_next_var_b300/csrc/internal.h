@@ -53,8 +53,11 @@ int encode_tmap_bf16(CUtensorMap* out, const void* base, int rank, const uint64_
 // Launchers: `status` is the device status word of the call.
 int launch_attn_dense(const StepGeom& g, const void* q, const void* k, const void* v, void* o,
                       cudaStream_t st, int32_t* status, float* lse = nullptr);
+// after_select: launch as a programmatic dependent of the pivot selection
+// kernel just launched on `st` (which lets it set up beside the selection).
 int launch_attn_pruned(const StepGeom& g, const void* q, const void* k, const void* v,
-                       const int32_t* idx, int keep_k, void* o, cudaStream_t st, int32_t* status, bool scatter);
+                       const int32_t* idx, int keep_k, void* o, cudaStream_t st, int32_t* status, bool scatter,
+                       bool after_select = false);
 int launch_attn_dense_halved(const StepGeom& g, const void* q, const void* k, const void* v, void* o,
                              cudaStream_t st, int32_t* status);
 int launch_attn_blocksparse(const StepGeom& g, const int32_t* sides, int n_scales, int step,

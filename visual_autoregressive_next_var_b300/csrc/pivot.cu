@@ -749,6 +749,9 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     const int b = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_wait();   // the scores of the score kernel
+    // a pruned attention chained after this kernel (var_pruned_step) may set up
+    // beside it now; it reads the index list only after this grid completes
+    pdl_launch_dependents();
     int32_t* out = idx_out + static_cast<size_t>(b) * K;
     if (K == N) {
         for (int j = tid; j < N; j += kSelThreads) out[j] = j;
