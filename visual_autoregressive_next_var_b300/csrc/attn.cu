@@ -70,6 +70,8 @@ template <int D, int MODE>
 static int launch_attn(const StepGeom& g, const void* q, const void* k, const void* v,
                        const int32_t* idx, int n_rows, void* o, cudaStream_t st, int32_t* status,
                        bool halved = false, bool scatter = false, float* lse = nullptr, bool pdl = false)
+// pdl: a programmatic dependent launch (only the gathered mode takes one; the
+// kernel waits for its predecessor after its set-up, before reading inputs)
 {
     using Lay = AttnLayout<D>;
     auto kern = attn_kernel<D, MODE, DenseMaps>;

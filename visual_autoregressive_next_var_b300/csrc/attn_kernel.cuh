@@ -326,9 +326,6 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::OFF_MISC + 4);
     const int2* U = reinterpret_cast<const int2*>(smem + Lay::OFF_U);
-    // in place (gathered rows scattered into the full grid): the fill of the
-    // other rows may start beside this grid; it reads and writes none of its rows
-    if (GATHER && args.scatter) pdl_launch_dependents();
 
     int bh, row0 = 0, by0 = 0, bx0 = 0;
     bool split = false;        // one query tile; group g takes key tiles j = g (mod 2)
@@ -405,6 +402,15 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Launched as a programmatic dependent (the gathered attention of
+    // var_pruned_step, behind the pivot selection), every thread waits here,
+    // after the set-up and before anything reads an input; an ordinary launch
+    // returns at once.
+    pdl_wait();
+    // In place (gathered rows scattered into the full grid): from here on the
+    // fill of the other rows may start beside this grid -- the indices are
+    // final, and it reads and writes none of this grid's rows.
+    if (GATHER && args.scatter) pdl_launch_dependents();
 
     int n_kv = args.n_kv;
     int n_units = 0;
@@ -609,10 +615,6 @@ __global__ void __launch_bounds__(384, 1) attn_kernel(const __grid_constant__ Ma
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax groups
-        // gathered rows: launched as a programmatic dependent of the pivot
-        // selection (var_pruned_step), the index list is read only once that
-        // grid has completed; a no-op for an ordinary launch
-        if constexpr (GATHER) pdl_wait();
         const int g = (warp - 4) >> 2;
         const int r = (warp & 3) * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
