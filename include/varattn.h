@@ -217,9 +217,9 @@ VAR_API int var_pruned_in_place(const var_problem* p, int32_t step, const void* 
  * only; "ARVAR" Key Design 2 and Key Design 3, Eq. (8)-(9)): var_pivot_select
  * of x (writing idx), then var_pruned_in_place with those indices, on
  * `stream`.  The pruned attention is launched as a programmatic dependent of
- * the selection kernel: its blocks set up and load keys and values beside the
- * selection and read idx once the selection has completed; the fill starts
- * beside the attention.  idx and out equal those of var_pivot_select followed
+ * the selection kernel: its blocks launch and set up beside the selection and
+ * read their inputs once it has completed; the fill then starts beside the
+ * attention.  idx and out equal those of var_pivot_select followed
  * by var_pruned_in_place (and so of the unfused chain).
  * x, channels, keep_k, idx, workspace: as var_pivot_select (no scores);
  * q, k, v, prev, out: as var_pruned_in_place.  keep_k = 0 writes the
