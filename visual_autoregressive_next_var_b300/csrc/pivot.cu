@@ -931,7 +931,9 @@ int launch_select_exact(int B, int N, int keep_k, const float* keys_lo, const fl
                                       : pivot_select_kernel<kMaxKeysPerThread>;
     const __nv_bfloat16* no_x = nullptr;
     const double* no_mean = nullptr;
-    return cuda_status(launch_kernel(fn, dim3(B), dim3(kSelThreads), 0, st, false, no_x, N, 32, keep_k, keys_lo,
+    // a programmatic dependent of the kernel that wrote the keys (it waits for
+    // that grid before reading them)
+    return cuda_status(launch_kernel(fn, dim3(B), dim3(kSelThreads), 0, st, true, no_x, N, 32, keep_k, keys_lo,
                                      keys_hi, no_mean, band_idx, band_score, idx, status, 1));
 }
 

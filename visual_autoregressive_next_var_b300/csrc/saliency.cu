@@ -241,6 +241,9 @@ __global__ void __launch_bounds__(256)
     guided_upsample_kernel(const float* __restrict__ sal, int H, int sp, int s, float ratio, float inv_hn,
                            float* __restrict__ lo, float* __restrict__ hi, float* __restrict__ scores)
 {
+    // the top-K kernel that follows (a programmatic dependent) may set up now;
+    // it reads lo / hi only after this grid has completed
+    pdl_launch_dependents();
     const int b = blockIdx.y;
     const int N = s * s, Np = sp * sp;
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
