@@ -249,10 +249,12 @@ def test_pruned_keep_all_equals_dense():
     check_device_status()
 
 
-def test_pruned_step_one_call_head_dim_64_ragged():
-    """var_pruned_step at head_dim 64 on a 23x23 grid: its indices equal the
-    oracle's pivots bit for bit and its output equals var_pivot_select +
-    var_attn_pruned + var_restore_scatter bit for bit."""
+@pytest.mark.parametrize("keep", [(1, 5), (1, 529), (1, 1)])
+def test_pruned_step_one_call_head_dim_64_ragged(keep):
+    """var_pruned_step at head_dim 64 on a 23x23 grid (keep 1/5, a single
+    token, every token): its indices equal the oracle's pivots bit for bit and
+    its output equals var_pivot_select + var_attn_pruned + var_restore_scatter
+    bit for bit."""
     sides, D, B, H, C_ = (1, 2, 4, 6, 9, 14, 20, 23), 64, 2, 3, 96
     step = len(sides) - 1
     L, N = cache_len(sides, step), sides[step] ** 2
@@ -260,7 +262,7 @@ def test_pruned_step_one_call_head_dim_64_ragged():
     prev_c = randn_bf16((B, H, 20 * 20, D), 194)
     x_c = randn_bf16((B, N, C_), 195)
     q, k, v, prev, x = qc.to(DEV), kc.to(DEV), vc.to(DEV), prev_c.to(DEV), x_c.to(DEV)
-    K = V.var_keep_count(N, 1, 5)
+    K = V.var_keep_count(N, *keep)
     p = V.problem(B, H, D, sides)
     ws = torch.empty(V.var_pivot_workspace_bytes(p, step, C_), dtype=torch.uint8, device=DEV)
     idx = torch.empty((B, K), dtype=torch.int32, device=DEV)
